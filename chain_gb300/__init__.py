@@ -1,0 +1,232 @@
+"""chain_gb300 -- Python binding of the sm_103a C-ABI library for O = f(A.B).C.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libchain_gb300.so`` (see ``include/chain.h``).  PyTorch is used
+for device memory and streams.  There is no fallback: if the library is
+missing or cannot be built, importing the binding's functions raises.
+
+Entry points (same names as the C ABI):
+  chain_fwd(A, B, C, f, mask, scale, O, LSE=None, stream=None)
+  chain_bwd(dO, A, B, C, O, LSE, f, mask, scale, dA, dB, dC, workspace, stream=None)
+  chain_bwd_workspace_size(A, C)
+  sp_relayout(shards, p, head_group, out, stream=None)
+  sp_relayout_inverse(inp, p, head_group, shards, stream=None)
+  chain_check(stream=None)
+plus allocating conveniences ``attention_fwd``, ``attention_bwd``,
+``mlp_chain_fwd`` and ``relayout``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+F_IDENTITY, F_SOFTMAX, F_GELU_TANH = 0, 1, 2
+MASK_NONE, MASK_CAUSAL = 0, 1
+BF16, F32 = 0, 1
+
+OK, ERR_ARG, ERR_DTYPE, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libchain_gb300.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class ChainError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = _load().chain_status_string(status).decode()
+        if status == ERR_CUDA:
+            msg += f" (cuda error {_load().chain_last_cuda_error()})"
+        super().__init__(f"{what}: {msg} [{status}]")
+
+
+class TensorDesc(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+def build(force: bool = False) -> str:
+    from . import _build
+    return _build.build(force=force)
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                build()
+            lib = ctypes.CDLL(LIB_PATH)
+            P = ctypes.POINTER(TensorDesc)
+            vp, ci, fl = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            lib.chain_fwd.argtypes = [P, P, P, ci, ci, fl, P, P, vp]
+            lib.chain_bwd.argtypes = [P, P, P, P, P, P, ci, ci, fl, P, P, P, vp, ctypes.c_size_t, vp]
+            lib.chain_bwd_workspace_size.argtypes = [P, P]
+            lib.chain_bwd_workspace_size.restype = ctypes.c_size_t
+            lib.sp_relayout.argtypes = [P, ci, ci, P, vp]
+            lib.sp_relayout_inverse.argtypes = [P, ci, ci, P, vp]
+            lib.chain_check.argtypes = [vp, ctypes.POINTER(ci)]
+            lib.chain_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            lib.chain_set_wait_limit_ns.restype = None
+            lib.chain_set_timing_events.argtypes = [vp, vp]
+            lib.chain_set_timing_events.restype = None
+            lib.chain_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+            lib.chain_umma_selftest.argtypes = [vp, vp, vp, ci, ci, ci, vp]
+            lib.chain_status_string.argtypes = [ci]
+            lib.chain_status_string.restype = ctypes.c_char_p
+            for fn in ("chain_fwd", "chain_bwd", "sp_relayout", "sp_relayout_inverse",
+                       "chain_check", "chain_selftest_wait_timeout", "chain_umma_selftest",
+                       "chain_last_cuda_error"):
+                getattr(lib, fn).restype = ci
+            _lib = lib
+    return _lib
+
+
+def lib():
+    return _load()
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.int16 or t.dtype == torch.float16:
+        return BF16  # 2-byte payload (relayout moves bits only)
+    if t.dtype == torch.int32:
+        return F32  # 4-byte payload
+    raise TypeError(f"chain_gb300: unsupported dtype {t.dtype}")
+
+
+def desc(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if t.dim() < 1 or t.dim() > 4:
+        raise ValueError("chain_gb300: tensors must have 1 to 4 dimensions")
+    d = TensorDesc()
+    d.ptr = t.data_ptr()
+    d.dtype = _dt(t)
+    d.ndim = t.dim()
+    for i, (s, st) in enumerate(zip(t.shape, t.stride())):
+        d.shape[i] = s
+        d.stride[i] = st
+    return d
+
+
+def _ref(d):
+    return ctypes.byref(d) if d is not None else None
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ok(rc: int, what: str):
+    if rc != OK:
+        raise ChainError(rc, what)
+
+
+# ------------------------------------------------------------- C-ABI calls
+def chain_fwd(A, B, C, f, mask, scale, O, LSE=None, stream=None):
+    """O = f(A B) C; see include/chain.h for shapes per f."""
+    _ok(_load().chain_fwd(_ref(desc(A)), _ref(desc(B)), _ref(desc(C)), int(f), int(mask),
+                          float(scale), _ref(desc(O)), _ref(desc(LSE)), _stream(stream)),
+        "chain_fwd")
+
+
+def chain_bwd_workspace_size(A, C) -> int:
+    return int(_load().chain_bwd_workspace_size(_ref(desc(A)), _ref(desc(C))))
+
+
+def chain_bwd(dO, A, B, C, O, LSE, f, mask, scale, dA, dB, dC, workspace, stream=None):
+    _ok(_load().chain_bwd(_ref(desc(dO)), _ref(desc(A)), _ref(desc(B)), _ref(desc(C)),
+                          _ref(desc(O)), _ref(desc(LSE)), int(f), int(mask), float(scale),
+                          _ref(desc(dA)), _ref(desc(dB)), _ref(desc(dC)),
+                          ctypes.c_void_p(workspace.data_ptr()),
+                          ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                          _stream(stream)), "chain_bwd")
+
+
+def sp_relayout(shards, p, head_group, out, stream=None):
+    _ok(_load().sp_relayout(_ref(desc(shards)), int(p), int(head_group), _ref(desc(out)),
+                            _stream(stream)), "sp_relayout")
+
+
+def sp_relayout_inverse(inp, p, head_group, shards, stream=None):
+    _ok(_load().sp_relayout_inverse(_ref(desc(inp)), int(p), int(head_group), _ref(desc(shards)),
+                                    _stream(stream)), "sp_relayout_inverse")
+
+
+def chain_check(stream=None) -> tuple[int, int]:
+    site = ctypes.c_int(0)
+    rc = _load().chain_check(_stream(stream), ctypes.byref(site))
+    return rc, site.value
+
+
+def set_wait_limit_ns(ns: int):
+    _load().chain_set_wait_limit_ns(int(ns))
+
+
+def set_timing_events(start=None, stop=None):
+    """Record torch.cuda.Event ``start``/``stop`` around the main kernel of
+    subsequent calls from this thread (None, None clears)."""
+    _load().chain_set_timing_events(
+        ctypes.c_void_p(start.cuda_event if start is not None else 0),
+        ctypes.c_void_p(stop.cuda_event if stop is not None else 0))
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None):
+    _ok(_load().chain_selftest_wait_timeout(int(limit_ns), _stream(stream)),
+        "chain_selftest_wait_timeout")
+
+
+def umma_selftest(A, B, D, N, K, b_mn_major, a_in_tmem=False, stream=None):
+    flags = int(bool(b_mn_major)) | (2 if a_in_tmem else 0)
+    _ok(_load().chain_umma_selftest(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
+                                    ctypes.c_void_p(D.data_ptr()), int(N), int(K), flags,
+                                    _stream(stream)), "chain_umma_selftest")
+
+
+# --------------------------------------------------- allocating helpers
+def attention_fwd(q, k, v, causal: bool, scale: float | None = None, stream=None):
+    """Returns (O, LSE) for q, k, v [BH, n, d] (or [B, H, n, d])."""
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    chain_fwd(q, k, v, F_SOFTMAX, MASK_CAUSAL if causal else MASK_NONE, scale, o, lse, stream)
+    return o, lse
+
+
+def attention_bwd(do, q, k, v, o, lse, causal: bool, scale: float | None = None,
+                  workspace=None, stream=None):
+    """Returns (dQ, dK, dV)."""
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    if workspace is None:
+        nbytes = chain_bwd_workspace_size(q, v)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    chain_bwd(do, q, k, v, o, lse, F_SOFTMAX, MASK_CAUSAL if causal else MASK_NONE, scale,
+              dq, dk, dv, workspace, stream)
+    return dq, dk, dv
+
+
+def mlp_chain_fwd(x, w1, w2, gelu: bool = True, stream=None):
+    """O = gelu_tanh(x w1) w2 (or (x w1) w2 with gelu=False)."""
+    o = torch.empty(x.shape[0], w2.shape[1], dtype=x.dtype, device=x.device)
+    chain_fwd(x, w1, w2, F_GELU_TANH if gelu else F_IDENTITY, MASK_NONE, 1.0, o, None, stream)
+    return o
+
+
+def relayout(shards, p: int, head_group: int, stream=None):
+    P, n_loc, H, d = shards.shape
+    out = torch.empty(H // p, p * n_loc, d, dtype=shards.dtype, device=shards.device)
+    sp_relayout(shards, p, head_group, out, stream)
+    return out

@@ -1,0 +1,428 @@
+// chain_api.cu -- the C ABI declared in include/chain.h: argument checks on
+// the host, dispatch to the kernels, tensor-map encoding, and the device
+// status word that bounded waits report into.
+#include <atomic>
+#include <mutex>
+
+#include "../../include/chain.h"
+#include "internal.h"
+
+namespace chain {
+
+// One status word per device, read by chain_check().
+__device__ DevStatus g_status;
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+thread_local cudaEvent_t t_ev_start = nullptr, t_ev_stop = nullptr;
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+
+struct DevInfo {
+  bool init = false;
+  bool ok = false;
+  int sms = 0;
+  DevStatus *status = nullptr;
+};
+constexpr int MAX_DEV = 64;
+DevInfo g_dev[MAX_DEV];
+std::mutex g_mu;
+
+// Signature of the driver's cuTensorMapEncodeTiled, resolved at run time
+// so the library needs no link-time dependency on libcuda.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return CHAIN_ERR_CUDA;
+}
+
+// Checks the current device (compute capability 10.3) and resolves the
+// status word's device address once per device.
+int device_ready(DevInfo **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= MAX_DEV) return CHAIN_ERR_DEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo &di = g_dev[dev];
+  if (!di.init) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+    di.ok = (major == 10 && minor == 3);
+    if (di.ok) {
+      void *addr = nullptr;
+      if ((e = cudaGetSymbolAddress(&addr, g_status)) != cudaSuccess) return cuda_fail(e);
+      di.status = static_cast<DevStatus *>(addr);
+      if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+          return cuda_fail(e != cudaSuccess ? e : cudaErrorNotSupported);
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+      }
+    }
+    di.init = true;
+  }
+  if (!di.ok) return CHAIN_ERR_DEVICE;
+  *out = &di;
+  return CHAIN_OK;
+}
+
+WaitCfg wait_cfg(const DevInfo *di) {
+  WaitCfg w;
+  w.status = di->status;
+  w.limit_ns = g_wait_limit_ns.load();
+  return w;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A [.., rows, cols] view: innermost stride 1, the others given.
+struct View {
+  void *ptr;
+  int dtype;
+  int64_t outer;   // product of leading dims (BH for attention)
+  int64_t rows;    // n or M
+  int64_t cols;    // d or K
+  int64_t s_outer; // elements between consecutive outer indices
+  int64_t s_row;   // elements between rows
+};
+
+int esize(int dtype) { return dtype == CHAIN_BF16 ? 2 : (dtype == CHAIN_F32 ? 4 : 0); }
+
+// Accepts 2-D [rows][cols], 3-D [BH][rows][cols] and 4-D [B][H][rows][cols]
+// where the two leading dims fold into one stride.
+int view_of(const chain_tensor_t *t, int min_nd, View *v) {
+  if (!t || !t->ptr) return CHAIN_ERR_ARG;
+  if (t->ndim < min_nd || t->ndim > 4) return CHAIN_ERR_ARG;
+  if (esize(t->dtype) == 0) return CHAIN_ERR_DTYPE;
+  const int nd = t->ndim;
+  for (int i = 0; i < nd; ++i)
+    if (t->shape[i] < 0 || t->stride[i] < 0) return CHAIN_ERR_ARG;
+  if (t->stride[nd - 1] != 1) return CHAIN_ERR_ARG;
+  v->ptr = t->ptr;
+  v->dtype = t->dtype;
+  v->cols = t->shape[nd - 1];
+  v->rows = nd >= 2 ? t->shape[nd - 2] : 1;
+  v->s_row = nd >= 2 ? t->stride[nd - 2] : v->cols;
+  if (nd <= 2) {
+    v->outer = 1;
+    v->s_outer = v->rows * v->s_row;
+  } else if (nd == 3) {
+    v->outer = t->shape[0];
+    v->s_outer = t->stride[0];
+  } else {
+    if (t->shape[1] > 1 && t->stride[0] != t->shape[1] * t->stride[1]) return CHAIN_ERR_ARG;
+    v->outer = t->shape[0] * t->shape[1];
+    v->s_outer = t->stride[1];
+  }
+  if (v->rows > 1 && v->s_row < v->cols) return CHAIN_ERR_ARG;
+  if (v->outer > 1 && v->s_outer < v->rows * v->s_row) return CHAIN_ERR_ARG;
+  return CHAIN_OK;
+}
+
+bool pitch16(const View &v) {
+  const int es = esize(v.dtype);
+  return aligned16(v.ptr) && ((v.s_row * es) % 16 == 0) && ((v.s_outer * es) % 16 == 0) &&
+         ((v.cols * es) % 16 == 0);
+}
+
+bool same_shape(const View &a, const View &b) {
+  return a.outer == b.outer && a.rows == b.rows && a.cols == b.cols;
+}
+
+// LSE [BH][n] (2-D), or [B][H][n] (3-D) folded, innermost contiguous.
+int lse_view(const chain_tensor_t *t, int64_t BH, int64_t n, int64_t *s_bh) {
+  if (!t || !t->ptr) return CHAIN_ERR_ARG;
+  if (t->dtype != CHAIN_F32) return CHAIN_ERR_DTYPE;
+  if (t->ndim < 1 || t->ndim > 3 || t->stride[t->ndim - 1] != 1) return CHAIN_ERR_ARG;
+  int64_t outer = 1;
+  for (int i = 0; i + 1 < t->ndim; ++i) outer *= t->shape[i];
+  if (t->shape[t->ndim - 1] != n || outer != BH) return CHAIN_ERR_ARG;
+  if (t->ndim == 1) {
+    *s_bh = n;
+  } else if (t->ndim == 2) {
+    *s_bh = t->stride[0];
+  } else {
+    if (t->shape[1] > 1 && t->stride[0] != t->shape[1] * t->stride[1]) return CHAIN_ERR_ARG;
+    *s_bh = t->stride[1];
+  }
+  if (BH > 1 && *s_bh < n) return CHAIN_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(t->ptr) & 3u) != 0) return CHAIN_ERR_ARG;
+  return CHAIN_OK;
+}
+
+}  // namespace
+
+void timing_mark_start(cudaStream_t st) {
+  if (t_ev_start) cudaEventRecord(t_ev_start, st);
+}
+void timing_mark_stop(cudaStream_t st) {
+  if (t_ev_stop) cudaEventRecord(t_ev_stop, st);
+}
+
+cudaError_t make_tmap(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void *base,
+                      const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box) {
+  if (!g_encode) return cudaErrorInitializationError;
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
+  CUresult r = g_encode(map, dt, (cuuint32_t)rank, const_cast<void *>(base), gd, gs, bx, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace chain
+
+using namespace chain;
+
+extern "C" {
+
+const char *chain_status_string(int status) {
+  switch (status) {
+    case CHAIN_OK: return "ok";
+    case CHAIN_ERR_ARG: return "invalid argument (pointer, shape, stride or alignment)";
+    case CHAIN_ERR_DTYPE: return "unsupported element type";
+    case CHAIN_ERR_DEVICE: return "current device is not compute capability 10.3";
+    case CHAIN_ERR_CUDA: return "CUDA call failed (see chain_last_cuda_error)";
+    case CHAIN_ERR_TIMEOUT: return "a bounded device-side wait expired";
+    case CHAIN_ERR_UNSUPPORTED: return "request not implemented by this build";
+    default: return "unknown status";
+  }
+}
+
+int chain_last_cuda_error(void) { return t_last_cuda_error; }
+
+void chain_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
+
+void chain_set_timing_events(void *start, void *stop) {
+  t_ev_start = static_cast<cudaEvent_t>(start);
+  t_ev_stop = static_cast<cudaEvent_t>(stop);
+}
+
+int chain_check(void *stream, int *detail) {
+  DevInfo *di = nullptr;
+  int rc = device_ready(&di);
+  if (rc != CHAIN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  DevStatus hs;
+  e = cudaMemcpyFromSymbol(&hs, g_status, sizeof hs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (detail) *detail = hs.site;
+  if (hs.timeout) {
+    DevStatus zero = {0, 0, {0, 0}};
+    e = cudaMemcpyToSymbol(g_status, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return CHAIN_ERR_TIMEOUT;
+  }
+  return CHAIN_OK;
+}
+
+int chain_selftest_wait_timeout(uint64_t limit_ns, void *stream) {
+  DevInfo *di = nullptr;
+  int rc = device_ready(&di);
+  if (rc != CHAIN_OK) return rc;
+  WaitCfg wc = wait_cfg(di);
+  wc.limit_ns = limit_ns ? limit_ns : 1;
+  cudaError_t e = launch_wait_selftest(wc, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
+}
+
+int chain_umma_selftest(const void *A, const void *B, float *D, int N, int K, int flags,
+                        void *stream) {
+  if (!A || !B || !D || (N != 64 && N != 128) || K <= 0 || K % 64 || K > 256)
+    return CHAIN_ERR_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(D)) return CHAIN_ERR_ARG;
+  DevInfo *di = nullptr;
+  int rc = device_ready(&di);
+  if (rc != CHAIN_OK) return rc;
+  cudaError_t e = launch_umma_selftest(A, B, D, N, K, flags & 3, wait_cfg(di),
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
+}
+
+int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B, const chain_tensor_t *C, int f,
+              int mask, float scale, chain_tensor_t *O, chain_tensor_t *LSE, void *stream) {
+  if (f != CHAIN_F_IDENTITY && f != CHAIN_F_SOFTMAX && f != CHAIN_F_GELU_TANH)
+    return CHAIN_ERR_ARG;
+  if (mask != CHAIN_MASK_NONE && mask != CHAIN_MASK_CAUSAL) return CHAIN_ERR_ARG;
+  View a, b, c, o;
+  int rc;
+  if ((rc = view_of(A, 2, &a)) || (rc = view_of(B, 2, &b)) || (rc = view_of(C, 2, &c)) ||
+      (rc = view_of(O, 2, &o)))
+    return rc;
+  if (a.dtype != b.dtype || a.dtype != c.dtype || a.dtype != o.dtype) return CHAIN_ERR_DTYPE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  if (f == CHAIN_F_SOFTMAX) {
+    if (!same_shape(a, b) || !same_shape(a, c) || !same_shape(a, o)) return CHAIN_ERR_ARG;
+    if (a.cols != 64 && a.cols != 128) return CHAIN_ERR_ARG;
+    if (a.rows < 1 || a.outer < 1) return CHAIN_ERR_ARG;
+    if (a.rows > (1 << 30) || a.outer > 65535 * 16) return CHAIN_ERR_ARG;
+    if (!(scale > 0.0f) || !(scale < 1e30f)) return CHAIN_ERR_ARG;
+    if (!pitch16(a) || !pitch16(b) || !pitch16(c) || !pitch16(o)) return CHAIN_ERR_ARG;
+    int64_t lse_sbh = 0;
+    if ((rc = lse_view(LSE, a.outer, a.rows, &lse_sbh))) return rc;
+    AttnFwdArgs args;
+    args.Q = a.ptr; args.K = b.ptr; args.V = c.ptr;
+    args.q_sbh = a.s_outer; args.q_srow = a.s_row;
+    args.k_sbh = b.s_outer; args.k_srow = b.s_row;
+    args.v_sbh = c.s_outer; args.v_srow = c.s_row;
+    args.O = o.ptr; args.o_sbh = o.s_outer; args.o_srow = o.s_row;
+    args.LSE = static_cast<float *>(LSE->ptr); args.lse_sbh = lse_sbh;
+    args.BH = (int)a.outer; args.n = (int)a.rows; args.d = (int)a.cols;
+    args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
+    DevInfo *di = nullptr;
+    if ((rc = device_ready(&di))) return rc;
+    cudaError_t e;
+    if (a.dtype == CHAIN_BF16) {
+      e = launch_attn_fwd_bf16(args, wait_cfg(di), st);
+    } else {
+      if (a.rows * a.outer > 65536) return CHAIN_ERR_UNSUPPORTED;
+      e = launch_attn_fwd_f32(args, wait_cfg(di), st);
+    }
+    if (e == cudaErrorNotSupported) return CHAIN_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
+  }
+
+  // MLP / identity chain: A [M][K], B [K][N], C [N][P], O [M][P], 2-D bf16.
+  if (mask != CHAIN_MASK_NONE) return CHAIN_ERR_ARG;
+  if (LSE && LSE->ptr) return CHAIN_ERR_ARG;
+  if (A->ndim != 2 || B->ndim != 2 || C->ndim != 2 || O->ndim != 2) return CHAIN_ERR_ARG;
+  if (a.dtype != CHAIN_BF16) return CHAIN_ERR_DTYPE;
+  if (a.cols != b.rows || b.cols != c.rows || o.rows != a.rows || o.cols != c.cols)
+    return CHAIN_ERR_ARG;
+  if (!pitch16(a) || !pitch16(b) || !pitch16(c) || !pitch16(o)) return CHAIN_ERR_ARG;
+  if (a.s_row != a.cols || b.s_row != b.cols || c.s_row != c.cols || o.s_row != o.cols)
+    return CHAIN_ERR_ARG;
+  MlpArgs m;
+  m.X = a.ptr; m.W1 = b.ptr; m.W2 = c.ptr; m.O = o.ptr;
+  m.M = (int)a.rows; m.K = (int)a.cols; m.N = (int)b.cols; m.P = (int)c.cols;
+  m.gelu = f == CHAIN_F_GELU_TANH;
+  if (m.M <= 0 || m.K <= 0 || m.N <= 0 || m.P <= 0) return CHAIN_ERR_ARG;
+  if (m.M % 128 || m.K % 128 || m.N % 128) return CHAIN_ERR_UNSUPPORTED;
+  if (!(m.P == 1024 || (m.P % 256 == 0 && m.P <= 1024))) return CHAIN_ERR_UNSUPPORTED;
+  DevInfo *di = nullptr;
+  if ((rc = device_ready(&di))) return rc;
+  cudaError_t e = launch_mlp_chain(m, wait_cfg(di), st);
+  if (e == cudaErrorNotSupported) return CHAIN_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
+}
+
+size_t chain_bwd_workspace_size(const chain_tensor_t *A, const chain_tensor_t *C) {
+  View a, c;
+  if (view_of(A, 2, &a) || view_of(C, 2, &c)) return 0;
+  if (!same_shape(a, c)) return 0;
+  const size_t acc = (size_t)a.outer * a.rows * a.cols * sizeof(float);
+  const size_t dvec = (size_t)a.outer * a.rows * sizeof(float);
+  return ((acc + 255) & ~size_t(255)) + ((dvec + 255) & ~size_t(255));
+}
+
+int chain_bwd(const chain_tensor_t *dO, const chain_tensor_t *A, const chain_tensor_t *B,
+              const chain_tensor_t *C, const chain_tensor_t *O, const chain_tensor_t *LSE, int f,
+              int mask, float scale, chain_tensor_t *dA, chain_tensor_t *dB, chain_tensor_t *dC,
+              void *workspace, size_t ws_bytes, void *stream) {
+  if (f != CHAIN_F_SOFTMAX) {
+    if (f == CHAIN_F_IDENTITY || f == CHAIN_F_GELU_TANH) return CHAIN_ERR_UNSUPPORTED;
+    return CHAIN_ERR_ARG;
+  }
+  if (mask != CHAIN_MASK_NONE && mask != CHAIN_MASK_CAUSAL) return CHAIN_ERR_ARG;
+  View g, q, k, v, o, dq, dk, dv;
+  int rc;
+  if ((rc = view_of(dO, 2, &g)) || (rc = view_of(A, 2, &q)) || (rc = view_of(B, 2, &k)) ||
+      (rc = view_of(C, 2, &v)) || (rc = view_of(O, 2, &o)) || (rc = view_of(dA, 2, &dq)) ||
+      (rc = view_of(dB, 2, &dk)) || (rc = view_of(dC, 2, &dv)))
+    return rc;
+  const View *all[8] = {&g, &q, &k, &v, &o, &dq, &dk, &dv};
+  for (const View *x : all) {
+    if (x->dtype != CHAIN_BF16) return CHAIN_ERR_DTYPE;
+    if (!same_shape(*x, q)) return CHAIN_ERR_ARG;
+    // the backward kernels take densely packed [BH][n][d]
+    if (x->s_row != x->cols || (x->outer > 1 && x->s_outer != x->rows * x->cols))
+      return CHAIN_ERR_ARG;
+    if (!aligned16(x->ptr)) return CHAIN_ERR_ARG;
+  }
+  if (q.cols != 64 && q.cols != 128) return CHAIN_ERR_ARG;
+  if (!(scale > 0.0f) || !(scale < 1e30f)) return CHAIN_ERR_ARG;
+  if (q.rows * q.cols * q.outer >= (int64_t(1) << 40)) return CHAIN_ERR_ARG;
+  int64_t lse_sbh = 0;
+  if ((rc = lse_view(LSE, q.outer, q.rows, &lse_sbh))) return rc;
+  if (lse_sbh != q.rows) return CHAIN_ERR_ARG;
+  const size_t need = chain_bwd_workspace_size(A, C);
+  if (!workspace || ws_bytes < need || !aligned16(workspace)) return CHAIN_ERR_ARG;
+  AttnBwdArgs args;
+  args.Q = q.ptr; args.K = k.ptr; args.V = v.ptr; args.O = o.ptr; args.dO = g.ptr;
+  args.LSE = static_cast<const float *>(LSE->ptr);
+  args.dQ = dq.ptr; args.dK = dk.ptr; args.dV = dv.ptr;
+  const size_t acc = (size_t)q.outer * q.rows * q.cols * sizeof(float);
+  args.dq_acc = static_cast<float *>(workspace);
+  args.Dvec = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                        ((acc + 255) & ~size_t(255)));
+  args.BH = (int)q.outer; args.n = (int)q.rows; args.d = (int)q.cols;
+  args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
+  DevInfo *di = nullptr;
+  if ((rc = device_ready(&di))) return rc;
+  cudaError_t e = launch_attn_bwd(args, wait_cfg(di), static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return CHAIN_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
+}
+
+static int relayout_common(const chain_tensor_t *seq, const chain_tensor_t *hm, int p, int g,
+                           int inverse, void *stream) {
+  if (!seq || !hm || !seq->ptr || !hm->ptr) return CHAIN_ERR_ARG;
+  if (seq->ndim != 4 || hm->ndim != 3) return CHAIN_ERR_ARG;
+  if (seq->dtype != hm->dtype || esize(seq->dtype) == 0) return CHAIN_ERR_DTYPE;
+  if (p <= 0 || g < 0 || g >= p) return CHAIN_ERR_ARG;
+  const int64_t P = seq->shape[0], n_loc = seq->shape[1], H = seq->shape[2], d = seq->shape[3];
+  if (P != p || n_loc <= 0 || H <= 0 || d <= 0 || H % p) return CHAIN_ERR_ARG;
+  const int64_t Hl = H / p;
+  if (hm->shape[0] != Hl || hm->shape[1] != p * n_loc || hm->shape[2] != d) return CHAIN_ERR_ARG;
+  // both sides densely packed
+  if (seq->stride[3] != 1 || seq->stride[2] != d || seq->stride[1] != H * d ||
+      seq->stride[0] != n_loc * H * d)
+    return CHAIN_ERR_ARG;
+  if (hm->stride[2] != 1 || hm->stride[1] != d || hm->stride[0] != p * n_loc * d)
+    return CHAIN_ERR_ARG;
+  const int64_t row_bytes = d * esize(seq->dtype);
+  if (row_bytes % 16 || !aligned16(seq->ptr) || !aligned16(hm->ptr)) return CHAIN_ERR_ARG;
+  if (p * n_loc * H * (row_bytes / 16) >= (int64_t(1) << 32)) return CHAIN_ERR_ARG;
+  DevInfo *di = nullptr;
+  int rc = device_ready(&di);
+  if (rc) return rc;
+  cudaError_t e = inverse ? launch_relayout(hm->ptr, seq->ptr, p, n_loc, H, row_bytes, g, 1,
+                                            static_cast<cudaStream_t>(stream))
+                          : launch_relayout(seq->ptr, hm->ptr, p, n_loc, H, row_bytes, g, 0,
+                                            static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
+}
+
+int sp_relayout(const chain_tensor_t *shards, int p, int head_group, chain_tensor_t *out,
+                void *stream) {
+  return relayout_common(shards, out, p, head_group, 0, stream);
+}
+
+int sp_relayout_inverse(const chain_tensor_t *in, int p, int head_group,
+                        chain_tensor_t *shards, void *stream) {
+  return relayout_common(shards, in, p, head_group, 1, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,63 @@
+// internal.h -- host-side declarations shared by the translation units of
+// the library (launchers and tensor-map helpers).  Not part of the ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sm103.cuh"
+
+namespace chain {
+
+// Encodes a 2-D/3-D bf16 or f32 tiled tensor map with 128-byte swizzle.
+// dims/strides are innermost first; strides (bytes) exclude the innermost.
+// Returns cudaSuccess or cudaErrorInvalidValue on encode failure.
+cudaError_t make_tmap(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void *base,
+                      const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box);
+
+struct AttnFwdArgs {
+  const void *Q, *K, *V;  // [BH][n][d]
+  int64_t q_sbh, q_srow, k_sbh, k_srow, v_sbh, v_srow;
+  void *O;
+  int64_t o_sbh, o_srow;
+  float *LSE;
+  int64_t lse_sbh;
+  int BH, n, d, causal;
+  float scale;
+};
+
+cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t st);
+cudaError_t launch_attn_fwd_f32(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t st);
+
+struct AttnBwdArgs {
+  const void *Q, *K, *V, *O, *dO;  // bf16 [BH][n][d], row stride d, head stride n*d
+  const float *LSE;                // [BH][n]
+  void *dQ, *dK, *dV;              // bf16 [BH][n][d]
+  float *dq_acc;                   // fp32 [BH][n][d] workspace
+  float *Dvec;                     // fp32 [BH][n] workspace
+  int BH, n, d, causal;
+  float scale;
+};
+cudaError_t launch_attn_bwd(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t st);
+
+struct MlpArgs {
+  const void *X, *W1, *W2;  // [M][K], [K][N], [N][P] bf16 row-major
+  void *O;                  // [M][P] bf16
+  int M, K, N, P;
+  int gelu;                 // 1 = gelu_tanh, 0 = identity
+};
+cudaError_t launch_mlp_chain(const MlpArgs &a, const WaitCfg &wc, cudaStream_t st);
+
+cudaError_t launch_relayout(const void *in, void *out, int64_t p, int64_t n_loc, int64_t H,
+                            int64_t row_bytes, int64_t g, int inverse, cudaStream_t st);
+
+// Measurement hook (chain_set_timing_events): record the calling thread's
+// start/stop events, if set, around the main kernel of a call.
+void timing_mark_start(cudaStream_t st);
+void timing_mark_stop(cudaStream_t st);
+
+cudaError_t launch_wait_selftest(const WaitCfg &wc, cudaStream_t st);
+cudaError_t launch_umma_selftest(const void *A, const void *B, float *D, int N, int K,
+                                 int flags, const WaitCfg &wc, cudaStream_t st);
+
+}  // namespace chain

@@ -1,0 +1,204 @@
+/*
+ * chain.h -- C ABI of the GB300 (sm_103a) library for the unit
+ *            O = f(A . B) . C
+ *
+ * The unit: two consecutive matrix products with a function between them,
+ * as named in the abstract of "Memory-efficient tensor parallelism"
+ * (FITEE 10.1631/FITEE.2400602).  Three instances are served:
+ *   - f = row softmax of scaled scores (attention: A = Q, B = K^T * scale,
+ *     C = V), causal or not, forward and a backward that recomputes the
+ *     scores from the saved log-sum-exp instead of storing them ("AutoSP:
+ *     Unlocking Long-Context LLM Training Via Compiler-Based Sequence
+ *     Parallelism", section 2.B);
+ *   - f = GeLU (tanh form), the MLP chain, whose [M][N] intermediate is
+ *     never written to memory;
+ *   - f = identity, O = (A B) C.
+ * plus the Ulysses sequence-shard -> head-major relayout that precedes
+ * attention ("Ulysses Sequence Parallelism", "Contexte Technique") and its
+ * inverse (the second exchange of "Analyse et Implications").
+ *
+ * Conventions common to every entry point
+ *  - Tensors are described by chain_tensor_t: a DEVICE pointer, an element
+ *    type, and shape/strides counted in ELEMENTS (not bytes), outermost
+ *    dimension first.  The innermost stride must be 1; every other stride
+ *    must describe a row-major layout without overlap.  Base pointers must
+ *    be 16-byte aligned and row pitches multiples of 16 bytes.
+ *  - Ownership: the caller allocates every buffer, including workspaces.
+ *    The library allocates no device memory, keeps no pointer after a call
+ *    returns, and does not synchronise: all work is enqueued on `stream`
+ *    (a cudaStream_t, NULL = the legacy default stream).
+ *  - Errors: 0 (CHAIN_OK) on success, a negative chain_status_t otherwise.
+ *    Argument errors are detected on the host before anything is enqueued.
+ *    CHAIN_ERR_CUDA keeps the CUDA error code, readable through
+ *    chain_last_cuda_error().  Device-side bounded waits that expire (a
+ *    pipeline that stopped making progress) do not trap: the kernel stops,
+ *    records the event in a device status word, and chain_check() returns
+ *    CHAIN_ERR_TIMEOUT after synchronising the stream.
+ *  - Thread safety: calls may be issued concurrently from several host
+ *    threads; the only global state is a per-device cache of attributes
+ *    guarded by a mutex.
+ */
+#ifndef CHAIN_GB300_H
+#define CHAIN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CHAIN_OK = 0,
+  CHAIN_ERR_ARG = -1,     /* null pointer, shape/stride mismatch, misalignment, bad size */
+  CHAIN_ERR_DTYPE = -2,   /* element type not supported for this call */
+  CHAIN_ERR_DEVICE = -3,  /* current device is not compute capability 10.3 */
+  CHAIN_ERR_CUDA = -4,    /* a CUDA runtime/driver call failed */
+  CHAIN_ERR_TIMEOUT = -5, /* a bounded device-side wait expired */
+  CHAIN_ERR_UNSUPPORTED = -6 /* valid request this build does not implement */
+} chain_status_t;
+
+typedef enum { CHAIN_BF16 = 0, CHAIN_F32 = 1 } chain_dtype_t;
+
+typedef enum {
+  CHAIN_F_IDENTITY = 0,  /* O = (A B) C */
+  CHAIN_F_SOFTMAX = 1,   /* O = softmax_row(scale * A B) C; attention */
+  CHAIN_F_GELU_TANH = 2  /* O = gelu_tanh(A B) C; MLP chain */
+} chain_f_t;
+
+typedef enum { CHAIN_MASK_NONE = 0, CHAIN_MASK_CAUSAL = 1 } chain_mask_t;
+
+typedef struct {
+  void *ptr;          /* device address of element [0, 0, ...] */
+  int32_t dtype;      /* chain_dtype_t */
+  int32_t ndim;       /* 1..4 */
+  int64_t shape[4];   /* elements, outermost first */
+  int64_t stride[4];  /* elements; stride[ndim-1] must be 1 */
+} chain_tensor_t;
+
+/*
+ * chain_fwd -- O = f(A B) C  (FITEE abstract: the unit METP partitions).
+ *
+ * f = CHAIN_F_SOFTMAX (attention):
+ *   A = Q [BH][n][d], B = K [BH][n][d] (passed untransposed; the product is
+ *   Q K^T), C = V [BH][n][d]; 3-D, or 4-D [B][H][n][d] (B*H folded).
+ *   d in {64, 128}; n >= 1.  bf16 in -> O bf16; f32 in -> O f32 (the small
+ *   full-precision variant, n*BH <= 65536).
+ *   S = scale * Q K^T (scale applied in fp32 to the fp32 product);
+ *   mask CAUSAL keeps keys j <= i on global positions (AutoSP 2.A item 4).
+ *   LSE [BH][n] f32 (required): LSE_i = ln sum_j exp(S_ij), natural log,
+ *   scale included.  O [BH][n][d].
+ * f = CHAIN_F_GELU_TANH or CHAIN_F_IDENTITY (MLP chain):
+ *   A [M][K], B [K][N], C [N][P] row-major bf16; O [M][P] bf16; LSE NULL;
+ *   scale and mask ignored (mask must be NONE).  Requires M, K, N multiples
+ *   of 128 and P == 1024 or a multiple of 256 up to 1024.  The [M][N]
+ *   intermediate is held on chip in 128 x 256 chunks and never written to
+ *   memory.  fp32 accumulation; intermediate rounded to bf16 before the
+ *   second product.
+ */
+int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B,
+              const chain_tensor_t *C, int f, int mask, float scale,
+              chain_tensor_t *O, chain_tensor_t *LSE, void *stream);
+
+/*
+ * chain_bwd_workspace_size -- bytes of device workspace chain_bwd needs for
+ * these shapes (an fp32 [BH][n][d] accumulator for dA plus an fp32 [BH][n]
+ * row term).  Returns 0 for invalid descriptors.
+ */
+size_t chain_bwd_workspace_size(const chain_tensor_t *A, const chain_tensor_t *C);
+
+/*
+ * chain_bwd -- gradients of the softmax chain (attention backward).
+ *   Inputs: dO, Q (A), K (B), V (C), O [BH][n][d] bf16 and LSE [BH][n] f32
+ *   as produced by chain_fwd with the same f, mask and scale.  Only
+ *   f = CHAIN_F_SOFTMAX with bf16 and d in {64, 128} is supported.
+ *   Outputs: dQ (dA), dK (dB), dV (dC) [BH][n][d] bf16.
+ *   S and P are recomputed per tile from LSE ("recompute, don't store",
+ *   AutoSP 2.B); D_i = sum_e dO_ie O_ie.
+ *   workspace: device buffer of at least chain_bwd_workspace_size() bytes,
+ *   16-byte aligned, contents ignored on entry.
+ */
+int chain_bwd(const chain_tensor_t *dO, const chain_tensor_t *A,
+              const chain_tensor_t *B, const chain_tensor_t *C,
+              const chain_tensor_t *O, const chain_tensor_t *LSE, int f,
+              int mask, float scale, chain_tensor_t *dA, chain_tensor_t *dB,
+              chain_tensor_t *dC, void *workspace, size_t ws_bytes,
+              void *stream);
+
+/*
+ * sp_relayout -- Ulysses sequence shards -> head-major for one head group
+ * ("Ulysses Sequence Parallelism", "Contexte Technique": every position of
+ * the sequence, a subset of the heads).
+ *   shards [p][n_loc][H][d]: shard s holds positions [s*n_loc, (s+1)*n_loc).
+ *   out    [H/p][p*n_loc][d]: out[h][s*n_loc+t][e] = shards[s][t][g*H/p+h][e]
+ *   with g = head_group in [0, p).  Bit-exact copy of any 2- or 4-byte
+ *   element type; d * element size must be a multiple of 16 bytes.
+ */
+int sp_relayout(const chain_tensor_t *shards, int p, int head_group,
+                chain_tensor_t *out, void *stream);
+
+/*
+ * sp_relayout_inverse -- head-major -> sequence shards (the second
+ * exchange of the Ulysses layer, "Analyse et Implications"):
+ *   shards[s][t][g*H/p+h][e] = in[h][s*n_loc+t][e]; the other heads of
+ *   `shards` are left untouched.  Same element and alignment rules.
+ */
+int sp_relayout_inverse(const chain_tensor_t *in, int p, int head_group,
+                        chain_tensor_t *shards, void *stream);
+
+/*
+ * chain_check -- synchronise `stream`, then read and clear the device
+ * status word.  Returns CHAIN_ERR_TIMEOUT if a bounded wait expired in any
+ * kernel since the last check, CHAIN_ERR_CUDA on a CUDA error, else 0.
+ * `detail` (may be NULL) receives the code of the wait site that expired.
+ */
+int chain_check(void *stream, int *detail);
+
+/*
+ * chain_set_wait_limit_ns -- limit of every device-side bounded wait
+ * (default 2e9 ns).  Takes effect for launches issued afterwards.
+ */
+void chain_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * chain_set_timing_events -- measurement hook.  While set (non-NULL), every
+ * chain_fwd / chain_bwd / sp_relayout call issued from the calling host
+ * thread records `start` (a cudaEvent_t) on its stream immediately before
+ * launching its main kernel and `stop` immediately after it, so the main
+ * kernel alone can be timed without the backward's preprocess and dQ
+ * conversion kernels.  Pass NULL, NULL to clear.  Events are owned by the
+ * caller.
+ */
+void chain_set_timing_events(void *start, void *stop);
+
+/*
+ * chain_selftest_wait_timeout -- launches one CTA that waits on a barrier
+ * nothing will ever complete, with the bounded wait of every kernel here,
+ * and returns after the wait expires.  chain_check() then reports
+ * CHAIN_ERR_TIMEOUT.  Exercises the failure path without faulting the GPU.
+ */
+int chain_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
+/*
+ * chain_umma_selftest -- diagnostic of the tensor-core building block:
+ * D[128][N] (f32) = A[128][K] . B, with A [128][K] bf16 row-major and B
+ * either [N][K] (flags bit 0 clear, i.e. D = A B^T) or [K][N] (bit 0 set),
+ * loaded by TMA into 128-byte-swizzled shared memory and multiplied by
+ * tcgen05.mma into tensor memory.  With flags bit 1 set, A is instead
+ * written into tensor memory by the threads (row i in lane i, two bf16 per
+ * column) and read from there by the MMA.  K in {64, 128, 192, 256},
+ * N in {64, 128}; all pointers are device addresses.
+ */
+int chain_umma_selftest(const void *A, const void *B, float *D, int N, int K,
+                        int flags, void *stream);
+
+/* Static description of a status code. */
+const char *chain_status_string(int status);
+
+/* CUDA error code of the most recent CHAIN_ERR_CUDA on this thread. */
+int chain_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CHAIN_GB300_H */
