@@ -131,54 +131,89 @@ class ClockSampler:
 class HotPath:
     """Buffers and calls of one step; every call goes through the C ABI."""
 
-    def __init__(self, dev, seed_shift=0):
+    def __init__(self, dev, seed_shift=0, only=None):
         import torch
         import chain_gb300 as cg
         import chain_synth as cs
         self.torch, self.cg, self.cs = torch, cg, cs
         self.dev = dev
+        self.only = only
         W = cs.WORKLOADS
         g = lambda k: W[k].seed + seed_shift
+        want = lambda key: only is None or only in key
+        e = torch.empty(0, device=dev)
         u = W["ulysses_128k"].dims
         self.u = u
-        self.shards = [cs.shard_inputs(u["p"], u["n_loc"], u["H"], u["d"], seed=g("ulysses_128k") + t,
-                                       device=dev) for t in range(3)]
         Hl, N = u["H"] // u["p"], u["p"] * u["n_loc"]
-        self.hm = [torch.empty(Hl, N, u["d"], dtype=torch.bfloat16, device=dev) for _ in range(3)]
-        self.o4 = torch.empty(Hl, N, u["d"], dtype=torch.bfloat16, device=dev)
-        self.l4 = torch.empty(Hl, N, dtype=torch.float32, device=dev)
+        if want("sp_relayout") or want("attn_fwd_causal_8x131072x128"):
+            self.shards = [cs.shard_inputs(u["p"], u["n_loc"], u["H"], u["d"],
+                                           seed=g("ulysses_128k") + t, device=dev) for t in range(3)]
+            self.hm = [torch.empty(Hl, N, u["d"], dtype=torch.bfloat16, device=dev) for _ in range(3)]
+            for t in range(3):
+                cg.sp_relayout(self.shards[t], u["p"], u["g"], self.hm[t])
+            self.o4 = torch.empty(Hl, N, u["d"], dtype=torch.bfloat16, device=dev)
+            self.l4 = torch.empty(Hl, N, dtype=torch.float32, device=dev)
+        else:
+            self.shards, self.hm, self.o4, self.l4 = [e] * 3, [e] * 3, e, e
         c3 = W["causal_attn_32k"].dims
         self.c3 = c3
-        self.q3, self.k3, self.v3 = cs.attn_inputs(c3["BH"], c3["n"], c3["d"], seed=g("causal_attn_32k"),
-                                                   device=dev)
-        self.o3 = torch.empty_like(self.q3)
-        self.l3 = torch.empty(c3["BH"], c3["n"], dtype=torch.float32, device=dev)
+        if want("attn_fwd_causal_32x32768x128"):
+            self.q3, self.k3, self.v3 = cs.attn_inputs(c3["BH"], c3["n"], c3["d"],
+                                                       seed=g("causal_attn_32k"), device=dev)
+            self.o3 = torch.empty_like(self.q3)
+            self.l3 = torch.empty(c3["BH"], c3["n"], dtype=torch.float32, device=dev)
+        else:
+            self.q3 = self.k3 = self.v3 = self.o3 = self.l3 = e
         m = W["gelu_mlp"].dims
         self.m = m
-        self.x, self.w1, self.w2 = cs.mlp_inputs(m["M"], m["K"], m["N"], m["P"], seed=g("gelu_mlp"),
-                                                 device=dev)
-        self.o2 = torch.empty(m["M"], m["P"], dtype=torch.bfloat16, device=dev)
+        if want("gelu_mlp"):
+            self.x, self.w1, self.w2 = cs.mlp_inputs(m["M"], m["K"], m["N"], m["P"],
+                                                     seed=g("gelu_mlp"), device=dev)
+            self.o2 = torch.empty(m["M"], m["P"], dtype=torch.bfloat16, device=dev)
+            self.mlp_ok = self._probe_mlp()
+        else:
+            self.x = self.w1 = self.w2 = self.o2 = e
+            self.mlp_ok = False
         b = W["causal_bwd_64k"].dims
         self.b = b
-        self.q5, self.k5, self.v5, self.do5 = cs.attn_inputs(b["BH"], b["n"], b["d"], seed=g("causal_bwd_64k"),
-                                                             device=dev, with_do=True)
-        # the forward that the backward consumes (outside the timed step)
-        self.o5, self.l5 = cg.attention_fwd(self.q5, self.k5, self.v5, True)
-        self.dq5, self.dk5, self.dv5 = (torch.empty_like(self.q5) for _ in range(3))
-        self.ws = torch.empty(cg.chain_bwd_workspace_size(self.q5, self.v5), dtype=torch.uint8,
-                              device=dev)
+        if want("attn_bwd"):
+            self.q5, self.k5, self.v5, self.do5 = cs.attn_inputs(
+                b["BH"], b["n"], b["d"], seed=g("causal_bwd_64k"), device=dev, with_do=True)
+            # the forward whose O and LSE the backward consumes (outside the step)
+            self.o5, self.l5 = cg.attention_fwd(self.q5, self.k5, self.v5, True)
+            self.dq5, self.dk5, self.dv5 = (torch.empty_like(self.q5) for _ in range(3))
+            self.ws = torch.empty(cg.chain_bwd_workspace_size(self.q5, self.v5), dtype=torch.uint8,
+                                  device=dev)
+        else:
+            self.q5 = self.k5 = self.v5 = self.do5 = self.o5 = self.l5 = e
+            self.dq5 = self.dk5 = self.dv5 = self.ws = e
         t1 = W["tiny_attn_fp32"].dims
         self.t1 = t1
-        self.q1, self.k1, self.v1 = cs.attn_inputs(t1["BH"], t1["n"], t1["d"], seed=g("tiny_attn_fp32"),
-                                                   dtype=torch.float32, device=dev)
-        self.o1 = torch.empty_like(self.q1)
-        self.l1 = torch.empty(t1["BH"], t1["n"], dtype=torch.float32, device=dev)
-        self.mlp_ok = self._probe_mlp()
-        self.comp = self._components()
+        if want("attn_fwd_fp32"):
+            self.q1, self.k1, self.v1 = cs.attn_inputs(t1["BH"], t1["n"], t1["d"],
+                                                       seed=g("tiny_attn_fp32"),
+                                                       dtype=torch.float32, device=dev)
+            self.o1 = torch.empty_like(self.q1)
+            self.l1 = torch.empty(t1["BH"], t1["n"], dtype=torch.float32, device=dev)
+            self.fp32_ok = self._probe_fp32()
+        else:
+            self.q1 = self.k1 = self.v1 = self.o1 = self.l1 = e
+            self.fp32_ok = False
+        self.comp = [c for c in self._components() if only is None or only in c["name"]]
 
     def _probe_mlp(self):
         try:
             self.cg.chain_fwd(self.x, self.w1, self.w2, self.cg.F_GELU_TANH, 0, 1.0, self.o2, None)
+            return True
+        except self.cg.ChainError as e:
+            if e.status == self.cg.ERR_UNSUPPORTED:
+                return False
+            raise
+
+    def _probe_fp32(self):
+        try:
+            self.cg.chain_fwd(self.q1, self.k1, self.v1, self.cg.F_SOFTMAX, 0,
+                              self.t1["d"] ** -0.5, self.o1, self.l1)
             return True
         except self.cg.ChainError as e:
             if e.status == self.cg.ERR_UNSUPPORTED:
@@ -191,31 +226,33 @@ class HotPath:
         Hl, N = u["H"] // u["p"], u["p"] * u["n_loc"]
         comps = []
         for t in range(3):
-            comps.append(dict(name=f"sp_relayout[{'QKV'[t]}]", flops=0.0,
+            comps.append(dict(name=f"sp_relayout[{'QKV'[t]}]", kernel="relayout_kernel", flops=0.0,
                               bytes=2.0 * Hl * N * u["d"] * 2, launches=1,
                               fn=(lambda t=t: cg.sp_relayout(self.shards[t], u["p"], u["g"], self.hm[t]))))
-        comps.append(dict(name="attn_fwd_causal_8x131072x128", flops=attn_fwd_flops(Hl, N, u["d"], True),
+        comps.append(dict(name="attn_fwd_causal_8x131072x128", kernel="attn_fwd_kernel", flops=attn_fwd_flops(Hl, N, u["d"], True),
                           bytes=0.0, launches=1,
                           fn=lambda: cg.chain_fwd(self.hm[0], self.hm[1], self.hm[2], cg.F_SOFTMAX,
                                                   cg.MASK_CAUSAL, u["d"] ** -0.5, self.o4, self.l4)))
-        comps.append(dict(name="attn_fwd_causal_32x32768x128",
+        comps.append(dict(name="attn_fwd_causal_32x32768x128", kernel="attn_fwd_kernel",
                           flops=attn_fwd_flops(c3["BH"], c3["n"], c3["d"], True), bytes=0.0, launches=1,
                           fn=lambda: cg.chain_fwd(self.q3, self.k3, self.v3, cg.F_SOFTMAX,
                                                   cg.MASK_CAUSAL, c3["d"] ** -0.5, self.o3, self.l3)))
         if self.mlp_ok:
-            comps.append(dict(name="gelu_mlp_4096x1024x4096x1024",
+            comps.append(dict(name="gelu_mlp_4096x1024x4096x1024", kernel="mlp_chain_kernel",
                               flops=mlp_flops(m["M"], m["K"], m["N"], m["P"]), bytes=0.0, launches=1,
                               fn=lambda: cg.chain_fwd(self.x, self.w1, self.w2, cg.F_GELU_TANH, 0, 1.0,
                                                       self.o2, None)))
-        comps.append(dict(name="attn_bwd_causal_16x65536x128",
+        comps.append(dict(name="attn_bwd_causal_16x65536x128", kernel="attn_bwd_kernel",
                           flops=attn_bwd_flops(b["BH"], b["n"], b["d"], True), bytes=0.0, launches=3,
                           fn=lambda: cg.chain_bwd(self.do5, self.q5, self.k5, self.v5, self.o5, self.l5,
                                                   cg.F_SOFTMAX, cg.MASK_CAUSAL, b["d"] ** -0.5,
                                                   self.dq5, self.dk5, self.dv5, self.ws)))
-        comps.append(dict(name="attn_fwd_fp32_1x256x64", flops=attn_fwd_flops(1, t1["n"], t1["d"], False),
-                          bytes=0.0, launches=1,
-                          fn=lambda: cg.chain_fwd(self.q1, self.k1, self.v1, cg.F_SOFTMAX, cg.MASK_NONE,
-                                                  t1["d"] ** -0.5, self.o1, self.l1)))
+        if self.fp32_ok:
+            comps.append(dict(name="attn_fwd_fp32_1x256x64", kernel="attn_fwd_f32_kernel",
+                              flops=attn_fwd_flops(1, t1["n"], t1["d"], False), bytes=0.0, launches=1,
+                              fn=lambda: cg.chain_fwd(self.q1, self.k1, self.v1, cg.F_SOFTMAX,
+                                                      cg.MASK_NONE, t1["d"] ** -0.5, self.o1,
+                                                      self.l1)))
         return comps
 
     def step(self, events=None):
@@ -233,6 +270,8 @@ class HotPath:
                              self.v5, self.do5, self.o5, self.l5, self.q1, self.k1, self.v1]
         outs = [self.o4, self.l4, self.o3, self.l3, self.o2, self.dq5, self.dk5, self.dv5, self.o1,
                 self.l1]
+        ins = [t for t in ins if t.numel() > 0]
+        outs = [t for t in outs if t.numel() > 0]
         h_in = [t.cpu().pin_memory() for t in ins]
         h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
         return ins, h_in, outs, h_out
@@ -274,9 +313,10 @@ def max_over_ranks(x, dist):
 
 
 # ------------------------------------------------------- CPU baseline
-def oracle_sample(budget_s=12.0):
-    """Time the fp64 oracle on a bounded sample of the same workloads; returns
-    (TFLOP/s, seconds, description, threads)."""
+def oracle_sample(scale: int = 1):
+    """Time the fp64 oracle on a bounded sample of the same workloads (about
+    15 s of host work at scale 1); returns (TFLOP/s, seconds, description,
+    threads)."""
     import torch
     import chain_synth as cs
     import oracle
@@ -285,29 +325,30 @@ def oracle_sample(budget_s=12.0):
     flops, secs, parts = 0.0, 0.0, []
     # attention forward rows of the 32k workload (one head), causal
     c3 = W["causal_attn_32k"].dims
-    q, k, v = cs.attn_inputs(1, c3["n"], c3["d"], seed=W["causal_attn_32k"].seed)
-    rows = [(0, r) for r in range(c3["n"] - 48, c3["n"])]
+    q, k, v = cs.attn_inputs(2, c3["n"], c3["d"], seed=W["causal_attn_32k"].seed)
+    nr = 6144 * scale
+    rows = [(h, r) for h in range(2) for r in range(c3["n"] - nr // 2, c3["n"])]
     t0 = time.perf_counter()
     oracle.softmax_fwd(q, k, v, c3["d"] ** -0.5, True, rows=rows)
     dt = time.perf_counter() - t0
     f = sum(4.0 * (r + 1) * c3["d"] for _, r in rows)
     flops, secs = flops + f, secs + dt
-    parts.append(f"attn fwd 48 rows of 32x32768x128 ({dt:.1f}s)")
+    parts.append(f"attn fwd {len(rows)} rows (last of 2 heads) of 32x32768x128 ({dt:.1f}s)")
     # backward: last 16 query rows of the 64k workload, one head
     b = W["causal_bwd_64k"].dims
     q, k, v, do = cs.attn_inputs(1, b["n"], b["d"], seed=W["causal_bwd_64k"].seed, with_do=True)
-    i0 = b["n"] - 16
+    i0 = b["n"] - 1536 * scale
     t0 = time.perf_counter()
     oracle.softmax_bwd(q, k, v, do, b["d"] ** -0.5, True, row_range=(i0, b["n"]),
                        col_range=(i0, b["n"]))
     dt = time.perf_counter() - t0
     f = sum(8.0 * (r + 1) * b["d"] for r in range(i0, b["n"]))
     flops, secs = flops + f, secs + dt
-    parts.append(f"attn bwd 16 rows of 16x65536x128 ({dt:.1f}s)")
+    parts.append(f"attn bwd {b['n'] - i0} rows of one head of 16x65536x128 ({dt:.1f}s)")
     # MLP rows
     m = W["gelu_mlp"].dims
     x, w1, w2 = cs.mlp_inputs(m["M"], m["K"], m["N"], m["P"], seed=W["gelu_mlp"].seed)
-    rows = list(range(0, m["M"], m["M"] // 32))
+    rows = list(range(0, m["M"]))
     t0 = time.perf_counter()
     oracle.chain_fwd(x, w1, w2, oracle.F_GELU_TANH, rows=rows)
     dt = time.perf_counter() - t0
@@ -367,9 +408,7 @@ def main():
     torch.cuda.set_device(dev)
     cg.lib()
     peaks, peak_src = load_peaks()
-    hp = HotPath(dev)
-    if args.only:
-        hp.comp = [c for c in hp.comp if args.only in c["name"]]
+    hp = HotPath(dev, only=args.only)
     stream = torch.cuda.current_stream()
 
     ncomp = len(hp.comp)
@@ -419,20 +458,34 @@ def main():
             e.update(GBps=round(gb, 1), frac_of_measured_hbm=round(gb / hbm_peak, 4),
                      frac_of_8TBps=round(gb / 8000.0, 4))
         components[c["name"]] = e
-    # dominant kernel: largest share of the step's device time
-    di = max(range(ncomp), key=lambda i: comp_ms[i])
-    dom = hp.comp[di]
+    # dominant kernel: the kernel function with the largest share of the
+    # step's device time; achieved = its algorithmic work / its time, summed
+    # over its launches in the step (one launch per component).
+    by_k = {}
+    for c, ms in zip(hp.comp, comp_ms):
+        k = by_k.setdefault(c["kernel"], {"ms": 0.0, "flops": 0.0, "bytes": 0.0, "launches": 0})
+        k["ms"] += ms
+        k["flops"] += c["flops"]
+        k["bytes"] += c["bytes"]
+        k["launches"] += 1
+    dom_name = max(by_k, key=lambda k: by_k[k]["ms"])
+    dom = by_k[dom_name]
+    share = dom["ms"] / sum(v["ms"] for v in by_k.values())
     if dom["flops"]:
-        ach = dom["flops"] / (comp_ms[di] * 1e-3) / 1e12
-        roof = {"kernel": dom["name"], "bound": "tensor", "achieved": round(ach, 1),
+        ach = dom["flops"] / (dom["ms"] * 1e-3) / 1e12
+        roof = {"kernel": dom_name, "bound": "tensor", "achieved": round(ach, 1),
                 "peak": tf_peak, "unit": "TFLOP/s", "frac": round(ach / tf_peak, 4),
                 "peak_source": f"{peak_src} bf16_tflops_sustained",
-                "per_launch_flops": dom["flops"], "traffic": None}
+                "launches_per_step": dom["launches"], "flops_per_step": dom["flops"],
+                "avg_launch_ms": round(dom["ms"] / dom["launches"], 4),
+                "share_of_step_device_time": round(share, 4), "traffic": None}
     else:
-        ach = dom["bytes"] / (comp_ms[di] * 1e-3) / 1e9
-        roof = {"kernel": dom["name"], "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
+        ach = dom["bytes"] / (dom["ms"] * 1e-3) / 1e9
+        roof = {"kernel": dom_name, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
                 "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "peak_source": f"{peak_src} hbm_gbs",
-                "per_launch_bytes": dom["bytes"], "traffic": None}
+                "launches_per_step": dom["launches"], "bytes_per_step": dom["bytes"],
+                "avg_launch_ms": round(dom["ms"] / dom["launches"], 4),
+                "share_of_step_device_time": round(share, 4), "traffic": None}
     flops_all = hp.flops * world
     value = flops_all / (ms_step * 1e-3) / 1e12
 

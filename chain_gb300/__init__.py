@@ -178,6 +178,9 @@ def set_wait_limit_ns(ns: int):
 def set_timing_events(start=None, stop=None):
     """Record torch.cuda.Event ``start``/``stop`` around the main kernel of
     subsequent calls from this thread (None, None clears)."""
+    for ev in (start, stop):
+        if ev is not None and ev.cuda_event == 0:
+            ev.record()  # torch creates the underlying event on first record
     _load().chain_set_timing_events(
         ctypes.c_void_p(start.cuda_event if start is not None else 0),
         ctypes.c_void_p(stop.cuda_event if stop is not None else 0))
