@@ -28,6 +28,8 @@ MASK_NONE, MASK_CAUSAL = 0, 1
 BF16, F32 = 0, 1
 
 OK, ERR_ARG, ERR_DTYPE, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
+ERR_SCRATCH_LIMIT = -7
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024  # CHAIN_NOALLOC_SCRATCH_BYTES
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libchain_gb300.so")
@@ -65,6 +67,7 @@ def _load():
             vp, ci, fl = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
             lib.chain_fwd.argtypes = [P, P, P, ci, ci, fl, P, P, vp]
             lib.chain_bwd.argtypes = [P, P, P, P, P, P, ci, ci, fl, P, P, P, vp, ctypes.c_size_t, vp]
+            lib.chain_bwd_noalloc.argtypes = [P, P, P, P, P, P, ci, ci, fl, P, P, P, vp]
             lib.chain_bwd_workspace_size.argtypes = [P, P]
             lib.chain_bwd_workspace_size.restype = ctypes.c_size_t
             lib.sp_relayout.argtypes = [P, ci, ci, P, vp]
@@ -78,7 +81,7 @@ def _load():
             lib.chain_umma_selftest.argtypes = [vp, vp, vp, ci, ci, ci, vp]
             lib.chain_status_string.argtypes = [ci]
             lib.chain_status_string.restype = ctypes.c_char_p
-            for fn in ("chain_fwd", "chain_bwd", "sp_relayout", "sp_relayout_inverse",
+            for fn in ("chain_fwd", "chain_bwd", "chain_bwd_noalloc", "sp_relayout", "sp_relayout_inverse",
                        "chain_check", "chain_selftest_wait_timeout", "chain_umma_selftest",
                        "chain_last_cuda_error"):
                 getattr(lib, fn).restype = ci
@@ -153,6 +156,16 @@ def chain_bwd(dO, A, B, C, O, LSE, f, mask, scale, dA, dB, dC, workspace, stream
                           ctypes.c_void_p(workspace.data_ptr()),
                           ctypes.c_size_t(workspace.numel() * workspace.element_size()),
                           _stream(stream)), "chain_bwd")
+
+
+def chain_bwd_noalloc(dO, A, B, C, O, LSE, f, mask, scale, dA, dB, dC, stream=None):
+    """chain_bwd without a workspace argument: the library's fixed scratch
+    array is used instead (see include/chain.h for the limit and the rules
+    on overlapping calls)."""
+    _ok(_load().chain_bwd_noalloc(_ref(desc(dO)), _ref(desc(A)), _ref(desc(B)), _ref(desc(C)),
+                                  _ref(desc(O)), _ref(desc(LSE)), int(f), int(mask), float(scale),
+                                  _ref(desc(dA)), _ref(desc(dB)), _ref(desc(dC)), _stream(stream)),
+        "chain_bwd_noalloc")
 
 
 def sp_relayout(shards, p, head_group, out, stream=None):

@@ -165,6 +165,8 @@ int lse_view(const chain_tensor_t *t, int64_t BH, int64_t n, int64_t *s_bh) {
 
 }  // namespace
 
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
 void timing_mark_start(cudaStream_t st) {
   if (t_ev_start) cudaEventRecord(t_ev_start, st);
 }
@@ -204,6 +206,8 @@ const char *chain_status_string(int status) {
     case CHAIN_ERR_CUDA: return "CUDA call failed (see chain_last_cuda_error)";
     case CHAIN_ERR_TIMEOUT: return "a bounded device-side wait expired";
     case CHAIN_ERR_UNSUPPORTED: return "request not implemented by this build";
+    case CHAIN_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than the fixed array of chain_bwd_noalloc";
     default: return "unknown status";
   }
 }

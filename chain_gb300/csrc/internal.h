@@ -51,6 +51,9 @@ cudaError_t launch_mlp_chain(const MlpArgs &a, const WaitCfg &wc, cudaStream_t s
 cudaError_t launch_relayout(const void *in, void *out, int64_t p, int64_t n_loc, int64_t H,
                             int64_t row_bytes, int64_t g, int inverse, cudaStream_t st);
 
+// Keeps `e` as the thread's last CUDA error and returns CHAIN_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
+
 // Measurement hook (chain_set_timing_events): record the calling thread's
 // start/stop events, if set, around the main kernel of a call.
 void timing_mark_start(cudaStream_t st);

@@ -55,7 +55,8 @@ typedef enum {
   CHAIN_ERR_DEVICE = -3,  /* current device is not compute capability 10.3 */
   CHAIN_ERR_CUDA = -4,    /* a CUDA runtime/driver call failed */
   CHAIN_ERR_TIMEOUT = -5, /* a bounded device-side wait expired */
-  CHAIN_ERR_UNSUPPORTED = -6 /* valid request this build does not implement */
+  CHAIN_ERR_UNSUPPORTED = -6, /* valid request this build does not implement */
+  CHAIN_ERR_SCRATCH_LIMIT = -7 /* problem needs more than CHAIN_NOALLOC_SCRATCH_BYTES */
 } chain_status_t;
 
 typedef enum { CHAIN_BF16 = 0, CHAIN_F32 = 1 } chain_dtype_t;
@@ -124,6 +125,40 @@ int chain_bwd(const chain_tensor_t *dO, const chain_tensor_t *A,
               int mask, float scale, chain_tensor_t *dA, chain_tensor_t *dB,
               chain_tensor_t *dC, void *workspace, size_t ws_bytes,
               void *stream);
+
+/*
+ * chain_bwd_noalloc -- chain_bwd for callers that cannot allocate device
+ * memory.  (An addition of this library: the method's write-ups have no
+ * counterpart.)
+ *
+ * chain_bwd needs a caller-provided scratch workspace.  Some callers have
+ * no way to provide one: a host program whose pool allocator reserved the
+ * device's memory up front and exposes no C handle to it, a plugin that must
+ * not grow the host process's device footprint after start-up, or a
+ * latency-bound loop that cannot afford cudaMalloc/cudaFree, which may
+ * synchronise the whole device.  This entry point takes the same arguments
+ * as chain_bwd minus the workspace and uses instead a fixed scratch array
+ * compiled into the library: CHAIN_NOALLOC_SCRATCH_BYTES (32 MiB) of device
+ * memory that every GPU which loads the library holds until the process
+ * exits.  It never calls cudaMalloc, cudaFree or any allocating routine.
+ *
+ * Limit: chain_bwd_workspace_size(A, C) must not exceed
+ * CHAIN_NOALLOC_SCRATCH_BYTES (for d = 128: BH * n <= 65,027 rows), else
+ * the call returns CHAIN_ERR_SCRATCH_LIMIT before enqueuing anything.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture begins.
+ * All calls on a device share the one array and leave their partial
+ * results in it; each call re-initialises what it reads.  Calls whose
+ * execution overlaps on the GPU (different streams, or host threads without
+ * ordering) race on the array and give wrong gradients: order them.
+ */
+#define CHAIN_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int chain_bwd_noalloc(const chain_tensor_t *dO, const chain_tensor_t *A,
+                      const chain_tensor_t *B, const chain_tensor_t *C,
+                      const chain_tensor_t *O, const chain_tensor_t *LSE, int f,
+                      int mask, float scale, chain_tensor_t *dA,
+                      chain_tensor_t *dB, chain_tensor_t *dC, void *stream);
 
 /*
  * sp_relayout -- Ulysses sequence shards -> head-major for one head group
