@@ -323,8 +323,7 @@ int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B, const chain_tens
   m.M = (int)a.rows; m.K = (int)a.cols; m.N = (int)b.cols; m.P = (int)c.cols;
   m.gelu = f == CHAIN_F_GELU_TANH;
   if (m.M <= 0 || m.K <= 0 || m.N <= 0 || m.P <= 0) return CHAIN_ERR_ARG;
-  if (m.M % 128 || m.K % 128 || m.N % 128) return CHAIN_ERR_UNSUPPORTED;
-  if (!(m.P == 1024 || (m.P % 256 == 0 && m.P <= 1024))) return CHAIN_ERR_UNSUPPORTED;
+  if (m.M % 128 || m.K % 64 || m.N % 128 || m.P % 256) return CHAIN_ERR_UNSUPPORTED;
   DevInfo *di = nullptr;
   if ((rc = device_ready(&di))) return rc;
   cudaError_t e = launch_mlp_chain(m, wait_cfg(di), st);

@@ -6,7 +6,4 @@ namespace chain {
 cudaError_t launch_attn_fwd_f32(const AttnFwdArgs &, const WaitCfg &, cudaStream_t) {
   return cudaErrorNotSupported;
 }
-cudaError_t launch_mlp_chain(const MlpArgs &, const WaitCfg &, cudaStream_t) {
-  return cudaErrorNotSupported;
-}
 }  // namespace chain

@@ -91,11 +91,12 @@ typedef struct {
  *   scale included.  O [BH][n][d].
  * f = CHAIN_F_GELU_TANH or CHAIN_F_IDENTITY (MLP chain):
  *   A [M][K], B [K][N], C [N][P] row-major bf16; O [M][P] bf16; LSE NULL;
- *   scale and mask ignored (mask must be NONE).  Requires M, K, N multiples
- *   of 128 and P == 1024 or a multiple of 256 up to 1024.  The [M][N]
- *   intermediate is held on chip in 128 x 256 chunks and never written to
- *   memory.  fp32 accumulation; intermediate rounded to bf16 before the
- *   second product.
+ *   scale and mask ignored (mask must be NONE).  Requires M and N
+ *   multiples of 128, K a multiple of 64, P a multiple of 256 (else
+ *   CHAIN_ERR_UNSUPPORTED).  The [M][N] intermediate is held on chip in
+ *   128 x 128 chunks and never written to memory.  fp32 accumulation; the
+ *   intermediate enters the second product as bf16 H_hi + bf16 residual
+ *   H_lo, so its rounding error is ~2^-16 relative.
  */
 int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B,
               const chain_tensor_t *C, int f, int mask, float scale,
