@@ -301,7 +301,7 @@ int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B, const chain_tens
     if (a.dtype == CHAIN_BF16) {
       e = launch_attn_fwd_bf16(args, wait_cfg(di), st);
     } else {
-      if (a.rows * a.outer > 65536) return CHAIN_ERR_UNSUPPORTED;
+      if (a.cols != 64) return CHAIN_ERR_UNSUPPORTED;
       e = launch_attn_fwd_f32(args, wait_cfg(di), st);
     }
     if (e == cudaErrorNotSupported) return CHAIN_ERR_UNSUPPORTED;

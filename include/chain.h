@@ -83,8 +83,11 @@ typedef struct {
  * f = CHAIN_F_SOFTMAX (attention):
  *   A = Q [BH][n][d], B = K [BH][n][d] (passed untransposed; the product is
  *   Q K^T), C = V [BH][n][d]; 3-D, or 4-D [B][H][n][d] (B*H folded).
- *   d in {64, 128}; n >= 1.  bf16 in -> O bf16; f32 in -> O f32 (the small
- *   full-precision variant, n*BH <= 65536).
+ *   n >= 1.  bf16 in -> O bf16, d in {64, 128}; O is accumulated from the
+ *   compensated pair P_hi + P_lo (bf16 head and residual of P) so the only
+ *   bf16 rounding is the output's.  f32 in -> O f32, d = 64 only (else
+ *   CHAIN_ERR_UNSUPPORTED): a small full-precision variant whose tensor-core
+ *   products split every operand into tf32 head + remainder (3 MMAs).
  *   S = scale * Q K^T (scale applied in fp32 to the fp32 product);
  *   mask CAUSAL keeps keys j <= i on global positions (AutoSP 2.A item 4).
  *   LSE [BH][n] f32 (required): LSE_i = ln sum_j exp(S_ij), natural log,

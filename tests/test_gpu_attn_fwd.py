@@ -106,3 +106,35 @@ def test_fwd_causal_32k_full_size_sampled(cg, orc):
     dm = wl.dims
     q, k, v = cs.attn_inputs(dm["BH"], dm["n"], dm["d"], seed=wl.seed)
     _sampled_check(cg, orc, q, k, v, True, seed=3, per_head=24)
+
+
+# ------------------------------------------------------- fp32 (3xTF32) path
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("BH,n", [(1, 256), (2, 300), (1, 1), (3, 129)])
+def test_fwd_fp32_vs_oracle(cg, orc, BH, n, causal):
+    q, k, v = cs.attn_inputs(BH, n, 64, seed=1000 + n, dtype=torch.float32)
+    o, lse = cg.attention_fwd(q.cuda(), k.cuda(), v.cuda(), causal, 0.125)
+    assert cg.chain_check()[0] == 0
+    assert o.dtype == torch.float32
+    ro, rl = orc.softmax_fwd(q, k, v, 0.125, causal)
+    mx, mean = assert_fwd_close(o, ro, f"fp32 {BH}x{n} causal={causal}")
+    assert mean < 1e-5, mean  # full fp32 accuracy from the split tf32 products
+    assert_lse_close(lse, rl, "fp32 LSE")
+
+
+def test_fwd_fp32_tiny_workload(cg, orc):
+    # 1 head, n = 256, d = 64, fp32 N(0,1), scale 1/8, non-causal
+    wl = cs.WORKLOADS["tiny_attn_fp32"]
+    dm = wl.dims
+    q, k, v = cs.attn_inputs(dm["BH"], dm["n"], dm["d"], seed=wl.seed, dtype=torch.float32)
+    o, lse = cg.attention_fwd(q.cuda(), k.cuda(), v.cuda(), False, 1.0 / math.sqrt(dm["d"]))
+    ro, rl = orc.softmax_fwd(q, k, v, 1.0 / math.sqrt(dm["d"]), False)
+    assert_fwd_close(o, ro, "tiny fp32 workload")
+    assert_lse_close(lse, rl, "tiny fp32 LSE")
+
+
+def test_fwd_fp32_rejects_d128(cg):
+    q = torch.zeros(1, 64, 128, dtype=torch.float32, device="cuda")
+    with pytest.raises(cg.ChainError) as ei:
+        cg.attention_fwd(q, q, q, False)
+    assert ei.value.status == cg.ERR_UNSUPPORTED
