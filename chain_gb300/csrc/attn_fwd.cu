@@ -6,56 +6,60 @@
 // tile by tile, never storing the n x n score matrix.  Causal masking keeps
 // keys j <= i on global positions (AutoSP, section 2.A item 4).
 //
-// One CTA per (head, 128-row query block), heaviest causal blocks first.
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread t owns query row t of the block.  Reads its
-//              row of S from tensor memory, runs the online softmax in fp32
-//              registers, and writes P as two bf16 tiles, P_hi = bf16(P)
-//              (round-to-nearest-even) and P_lo = bf16(P - P_hi), into
-//              128-byte-swizzled shared memory; O accumulates P_hi V + P_lo V,
-//              so rounding the intermediate costs ~2^-16 relative instead of
-//              2^-9 and the only bf16 rounding left is the output's.  It
-//              rescales O in tensor memory when its running max grew by more
-//              than 2^8, and finally writes O / l (bf16) and LSE.
-//   warp 4     TMA producer: Q once, then K_j and V_j into a 2-stage ring
-//              (the on-chip form of METP's double buffer).
-//   warp 5     MMA issuer: S_j = Q K_j^T into one of two tensor-memory S
-//              buffers, then O += (P_hi + P_lo)_{j-1} V_{j-1}; completion is signalled
-//              with tcgen05.commit onto mbarriers.
-// Tensor memory: S0 [0,128), S1 [128,256), O [256, 256+d).
+// One CTA per (head, 256-row query block) = two 128-row query tiles "a" and
+// "b" that share every K/V tile, heaviest causal blocks first.
+// Warp roles (320 threads):
+//   warps 0-3  softmax of tile a, warps 4-7 softmax of tile b: thread t of
+//              a warpgroup owns query row t of its tile.  It reads its row
+//              of S from tensor memory, runs the online softmax in fp32
+//              registers and writes P back into the same tensor-memory
+//              columns as a compensated pair, P_hi = bf16(P) (round to
+//              nearest even) and P_lo = bf16(P - P_hi): keys [16k, 16k+16)
+//              occupy columns [16k, 16k+8) (P_hi) and [16k+8, 16k+16)
+//              (P_lo), two keys per 32-bit column.  O then accumulates
+//              P_hi V + P_lo V, so the only bf16 rounding left is the
+//              output's.  O is rescaled in tensor memory only when the row
+//              max grew by more than 2^8 since the last rescale.
+//   warp 8     TMA producer: Q_a and Q_b once, then K_j and V_j into 2-stage
+//              rings (the on-chip form of METP's double buffer).
+//   warp 9     MMA issuer, in the order  PV_a(j), S_a(j+1), PV_b(j), S_b(j+1):
+//              while one warpgroup exponentiates, the tensor core multiplies
+//              for the other.  The MMAs of one thread execute in issue order,
+//              so completion of S_t(j+1) implies PV_t(j) is done and
+//              P_t(j+1) may overwrite P_t(j) as soon as S_t(j+1) is read.
+// Tensor memory: S_a/P_a [0,128), S_b/P_b [128,256), O_a [256,384),
+// O_b [384,512).
 #include "internal.h"
 
 namespace chain {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 128;
+constexpr int BM = 128;  // rows per query tile (two tiles per CTA)
+constexpr int BN = 128;  // keys per K/V tile
 constexpr int STAGES = 2;
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 320;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 
 template <int D>
 struct FwdLayout {
   static constexpr uint32_t Q_BYTES = BM * D * 2;
   static constexpr uint32_t KV_BYTES = BN * D * 2;
-  static constexpr uint32_t P_TILE = BM * BN * 2;  // one bf16 [128][128] tile
-  static constexpr uint32_t P_BYTES = 2 * P_TILE;    // P_hi, P_lo
-  static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
+  static constexpr uint32_t OFF_Q = 0;                        // Q_a, Q_b
+  static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_BYTES;      // STAGES
   static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr uint32_t OFF_P = OFF_V + STAGES * KV_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
-  static constexpr uint32_t NBAR = 1 + 3 * STAGES + 2 + 2 + 1 + 1 + 1;
+  static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
+  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2],
+  // p_ready[2], pv_done[2], mma_drain
+  static constexpr uint32_t NBAR = 1 + 4 * STAGES + 2 + 2 + 2 + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16;
-  // Dynamic shared memory requested: the layout plus slack to align the
-  // base to 1024 bytes, and at least enough to keep one CTA per SM (the
-  // kernel allocates all 512 tensor-memory columns).
+  // At least enough shared memory to keep one CTA per SM: the kernel holds
+  // all 512 tensor-memory columns.
   static constexpr uint32_t ALLOC = (BYTES + 1024 > 120 * 1024) ? BYTES + 1024 : 120 * 1024;
 };
 
 struct FwdParams {
-  int BH, n, nqb, nkb, causal;
+  int BH, n, nqb2, nkb, causal;
   float scale_log2;
   __nv_bfloat16 *O;
   int64_t o_sbh, o_srow;
@@ -79,6 +83,13 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const
   mbar_wait(bar, parity, wc, &never, SITE_FWD_DRAIN);
 }
 
+// Number of key tiles query tile t (0 = a, 1 = b) of 256-row block qb sees.
+__device__ __forceinline__ int kv_tiles(const FwdParams &p, int qb, int t) {
+  if (!p.causal) return p.nkb;
+  const int last = 2 * qb + t + 1;  // tiles 0..2qb+t hold keys <= the tile's rows
+  return last < p.nkb ? last : p.nkb;
+}
+
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -91,45 +102,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
   uint64_t *q_full = bars;
   uint64_t *k_full = bars + 1;
-  uint64_t *v_full = k_full + STAGES;
-  uint64_t *kv_empty = v_full + STAGES;
-  uint64_t *s_full = kv_empty + STAGES;
-  uint64_t *s_free = s_full + 2;
-  uint64_t *p_full = s_free + 2;
-  uint64_t *pv_done = p_full + 1;
-  uint64_t *mma_drain = pv_done + 1;
+  uint64_t *k_empty = k_full + STAGES;
+  uint64_t *v_full = k_empty + STAGES;
+  uint64_t *v_empty = v_full + STAGES;
+  uint64_t *s_full = v_empty + STAGES;  // [2]
+  uint64_t *p_ready = s_full + 2;       // [2]
+  uint64_t *pv_done = p_ready + 2;      // [2]
+  uint64_t *mma_drain = pv_done + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int blk = blockIdx.x;
-  const int qb = p.causal ? (p.nqb - 1 - blk / p.BH) : (blk / p.BH);
+  const int qb = p.causal ? (p.nqb2 - 1 - blk / p.BH) : (blk / p.BH);
   const int bh = blk % p.BH;
-  const int nkv = p.causal ? (qb + 1) : p.nkb;
+  const int nkv_a = kv_tiles(p, qb, 0);
+  const int nkv_b = kv_tiles(p, qb, 1);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 128);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_ready[t], 128);
+      mbar_init(&pv_done[t], 1);
     }
-    mbar_init(p_full, 128);
-    mbar_init(pv_done, 1);
     mbar_init(mma_drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -139,42 +151,49 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued = 0;
-      mbar_arrive_expect_tx(q_full, L::Q_BYTES);
+      int k_issued = 0, v_issued = 0;
+      mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(smem + L::OFF_Q + c * (BM * 128), &tmQ, q_full, c * 64, qb * BM, bh);
-      for (int j = 0; j < nkv; ++j) {
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + L::OFF_Q + t * L::Q_BYTES + c * (BM * 128), &tmQ, q_full, c * 64,
+                      (2 * qb + t) * BM, bh);
+      for (int j = 0; j < nkv_b; ++j) {
         const int st = j % STAGES;
         if (j >= STAGES &&
-            !mbar_wait(&kv_empty[st], ((j / STAGES) - 1) & 1, p.wc, abort_flag, SITE_FWD_PROD))
+            !mbar_wait(&k_empty[st], ((j / STAGES) - 1) & 1, p.wc, abort_flag, SITE_FWD_PROD))
           break;
         mbar_arrive_expect_tx(&k_full[st], L::KV_BYTES);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(smem + L::OFF_K + st * L::KV_BYTES + c * (BN * 128), &tmK, &k_full[st],
                       c * 64, j * BN, bh);
+        k_issued = j + 1;
+        if (j >= STAGES &&
+            !mbar_wait(&v_empty[st], ((j / STAGES) - 1) & 1, p.wc, abort_flag, SITE_FWD_PROD))
+          break;
         mbar_arrive_expect_tx(&v_full[st], L::KV_BYTES);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(smem + L::OFF_V + st * L::KV_BYTES + c * (BN * 128), &tmV, &v_full[st],
                       c * 64, j * BN, bh);
-        issued = j + 1;
+        v_issued = j + 1;
       }
       if (*abort_flag) {
         // Let every copy still in flight land before shared memory is freed.
         drain_wait(q_full, 0, p.wc);
-        for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j) {
+        for (int j = (k_issued > STAGES ? k_issued - STAGES : 0); j < k_issued; ++j)
           drain_wait(&k_full[j % STAGES], (j / STAGES) & 1, p.wc);
+        for (int j = (v_issued > STAGES ? v_issued - STAGES : 0); j < v_issued; ++j)
           drain_wait(&v_full[j % STAGES], (j / STAGES) & 1, p.wc);
-        }
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
@@ -182,46 +201,66 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t sQ = smem_u32(smem + L::OFF_Q);
       const uint32_t sK = smem_u32(smem + L::OFF_K);
       const uint32_t sV = smem_u32(smem + L::OFF_V);
-      const uint32_t sP = smem_u32(smem + L::OFF_P);
-      if (mbar_wait(q_full, 0, p.wc, abort_flag, SITE_FWD_MMA)) {
-        for (int j = 0; j <= nkv; ++j) {
-          if (j < nkv) {
-            const int st = j % STAGES, sb = j & 1;
-            if (!mbar_wait(&k_full[st], (j / STAGES) & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
-            if (j >= 2 &&
-                !mbar_wait(&s_free[sb], ((j >> 1) - 1) & 1, p.wc, abort_flag, SITE_FWD_MMA))
-              break;
+      // S_t(j) = Q_t K_j^T into columns [128t, 128t+128)
+      auto issue_s = [&](int t, int j) {
+        const int st = j % STAGES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          umma_f16_ss(tmem + t * BN, sdesc_sw128(sQ + t * L::Q_BYTES + off, 16, 1024),
+                      sdesc_sw128(sK + st * L::KV_BYTES + (kk >> 2) * (BN * 128) + (kk & 3) * 32,
+                                  16, 1024),
+                      idS, kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_t += P_hi V_j + P_lo V_j, P read from tensor memory
+      auto issue_pv = [&](int t, int j) {
+        const int st = j % STAGES;
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            umma_f16_ts(tmem + 256 + t * 128, tmem + t * BN + kk * 16 + part * 8,
+                        sdesc_sw128(sV + st * L::KV_BYTES + kk * 2048, BN * 128, 1024), idO,
+                        (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(q_full, 0, p.wc, abort_flag, SITE_FWD_MMA) &&
+                mbar_wait(&k_full[0], 0, p.wc, abort_flag, SITE_FWD_MMA);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        umma_commit(&s_full[0]);
+        issue_s(1, 0);
+        umma_commit(&s_full[1]);
+        umma_commit(&k_empty[0]);
+      }
+      for (int j = 0; ok && j < nkv_b; ++j) {
+        const int st = j % STAGES;
+        const int jn = j + 1, stn = jn % STAGES;
+        if (!mbar_wait(&v_full[st], (j / STAGES) & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
+        if (j < nkv_a) {
+          if (!mbar_wait(&p_ready[0], j & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
+          tc_fence_after();
+          issue_pv(0, j);
+          umma_commit(&pv_done[0]);
+          if (jn < nkv_a) {
+            if (!mbar_wait(&k_full[stn], (jn / STAGES) & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-              const uint64_t a = sdesc_sw128(sQ + off, 16, 1024);
-              const uint64_t b =
-                  sdesc_sw128(sK + st * L::KV_BYTES + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16,
-                              1024);
-              umma_f16_ss(tmem + sb * BN, a, b, idS, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(&s_full[sb]);
+            issue_s(0, jn);
+            umma_commit(&s_full[0]);
           }
-          if (j >= 1) {
-            const int jp = j - 1, st = jp % STAGES;
-            if (!mbar_wait(p_full, jp & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
-            if (!mbar_wait(&v_full[st], (jp / STAGES) & 1, p.wc, abort_flag, SITE_FWD_MMA))
-              break;
-            tc_fence_after();
-#pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-              for (int kk = 0; kk < BN / 16; ++kk) {
-                const uint64_t a = sdesc_sw128(
-                    sP + part * L::P_TILE + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024);
-                const uint64_t b =
-                    sdesc_sw128(sV + st * L::KV_BYTES + kk * 2048, BN * 128, 1024);
-                umma_f16_ss(tmem + 2 * BN, a, b, idO, (jp > 0 || part > 0 || kk > 0) ? 1u : 0u);
-              }
-            umma_commit(pv_done);
-            umma_commit(&kv_empty[st]);
-          }
+        }
+        if (!mbar_wait(&p_ready[1], j & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
+        tc_fence_after();
+        issue_pv(1, j);
+        umma_commit(&pv_done[1]);
+        umma_commit(&v_empty[st]);
+        if (jn < nkv_b) {
+          if (!mbar_wait(&k_full[stn], (jn / STAGES) & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
+          tc_fence_after();
+          issue_s(1, jn);
+          umma_commit(&s_full[1]);
+          umma_commit(&k_empty[stn]);
         }
       }
       // No MMA may still be running when tensor memory is released.
@@ -231,37 +270,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int row = threadIdx.x;  // 0..127, TMEM lane = row
-    const int q_idx = qb * BM + row;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int t = warp >> 2;            // query tile of this warpgroup
+    const int row = threadIdx.x & 127;  // tensor-memory lane = row
+    const int q_idx = (2 * qb + t) * BM + row;
+    const int nkv = t ? nkv_b : nkv_a;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + t * BN;
+    const uint32_t tO = tmem + lane_off + 256 + t * 128;
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, p.wc, abort_flag, SITE_FWD_SOFTMAX)) {
+      if (!mbar_wait(&s_full[t], j & 1, p.wc, abort_flag, SITE_FWD_SOFTMAX)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t s[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c)
-        tmem_ld32(tmem + lane_off + sb * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&s_free[sb]);
-
       const int kv0 = j * BN;
-      const bool diag = p.causal && (j == qb);
-      const bool tail = (kv0 + BN > p.n);
+      const bool diag = p.causal && (j == 2 * qb + t);
+      const bool masked = diag || (kv0 + BN > p.n);
+      // pass 1: row max (32 columns at a time; diagonal and ragged tiles
+      // mask keys after the row and keys beyond n)
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        float v = __uint_as_float(s[c]) * p.scale_log2;
-        if ((diag && kv0 + c > q_idx) || (tail && kv0 + c >= p.n)) v = -INFINITY;
-        s[c] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t s[32];
+        tmem_ld32(tS + c * 32, s);
+        tmem_wait_ld();
+        if (masked) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int kv = kv0 + c * 32 + k;
+            if ((diag && kv > q_idx) || kv >= p.n) s[k] = __float_as_uint(-INFINITY);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) mx = fmaxf(mx, __uint_as_float(s[k]));
       }
+      mx *= p.scale_log2;  // scale > 0: the max commutes with the scaling
       float alpha = 1.0f;
       bool rescale = false;
       if (j == 0) {
@@ -272,64 +317,63 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         rescale = true;
       }
       const float mref = (m == -INFINITY) ? 0.0f : m;
-      float rs = 0.0f;
-      uint32_t pk[BN / 2], pl[BN / 2];
+      // O_t holds every P_t(j') V_j' with j' < j here: S_t(j) was issued
+      // after PV_t(j-1), and PV_t(j) waits for p_ready below.
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < BN; c += 2) {
-        const float p0 = ex2(__uint_as_float(s[c]) - mref);
-        const float p1 = ex2(__uint_as_float(s[c + 1]) - mref);
-        rs += p0 + p1;
-        const uint32_t h = pack_bf16(p0, p1);
-        pk[c / 2] = h;
-        pl[c / 2] = pack_bf16(p0 - __uint_as_float(h << 16), p1 - __uint_as_float(h & 0xffff0000u));
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
+      }
+      // pass 2: P = 2^(s*scale*log2e - m) for 32 keys at a time, written
+      // back over the columns just read: keys [16k, 16k+16) go to columns
+      // [16k, 16k+8) (P_hi) and [16k+8, 16k+16) (P_lo), two keys per column.
+      float rs = 0.0f;
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t s[32];
+        tmem_ld32(tS + c * 32, s);
+        tmem_wait_ld();
+        if (masked) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int kv = kv0 + c * 32 + k;
+            if ((diag && kv > q_idx) || kv >= p.n) s[k] = __float_as_uint(-INFINITY);
+          }
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(s[k]), p.scale_log2, -mref));
+          const float p1 = ex2(fmaf(__uint_as_float(s[k + 1]), p.scale_log2, -mref));
+          rs += p0 + p1;
+          const uint32_t h = pack_bf16(p0, p1);
+          const int g = k >> 4, w = (k & 15) >> 1;  // 16-key group, pair within it
+          pk[g * 16 + w] = h;
+          pk[g * 16 + 8 + w] =
+              pack_bf16(p0 - __uint_as_float(h << 16), p1 - __uint_as_float(h & 0xffff0000u));
+        }
+        tmem_st32(tS + c * 32, pk);
       }
       l = l * alpha + rs;
-
-      if (j > 0) {
-        if (!mbar_wait(pv_done, (j - 1) & 1, p.wc, abort_flag, SITE_FWD_SOFTMAX)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            const uint32_t ta = tmem + lane_off + 2 * BN + c * 32;
-            tmem_ld32(ta, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            tmem_st32(ta, o);
-          }
-          tmem_wait_st();
-        }
-      }
-      // P into the 128-byte-swizzled K-major tile: half h holds keys
-      // [64h, 64h+64) of every row, 8 chunks of 16 bytes per row.
-      const uint32_t sP = smem_u32(smem + L::OFF_P);
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const int b = h * 32 + ch * 4;
-          const uint32_t off = h * (BM * 128) + sw128_off(row, ch);
-          st_shared_v4(sP + off, pk[b], pk[b + 1], pk[b + 2], pk[b + 3]);
-          st_shared_v4(sP + L::P_TILE + off, pl[b], pl[b + 1], pl[b + 2], pl[b + 3]);
-        }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_ready[t]);
     }
     // ----------------------------------------------------------- epilogue
-    if (ok && mbar_wait(pv_done, (nkv - 1) & 1, p.wc, abort_flag, SITE_FWD_EPI)) {
+    if (ok && mbar_wait(&pv_done[t], (nkv - 1) & 1, p.wc, abort_flag, SITE_FWD_EPI)) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
       __nv_bfloat16 *orow = p.O + (int64_t)bh * p.o_sbh + (int64_t)q_idx * p.o_srow;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + 2 * BN + c * 32, o);
+        tmem_ld32(tO + c * 32, o);
         tmem_wait_ld();
         if (q_idx < p.n) {
           uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
@@ -351,7 +395,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -376,7 +420,7 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t s
   FwdParams p;
   p.BH = a.BH;
   p.n = a.n;
-  p.nqb = (a.n + BM - 1) / BM;
+  p.nqb2 = (a.n + 2 * BM - 1) / (2 * BM);
   p.nkb = (a.n + BN - 1) / BN;
   p.causal = a.causal;
   p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -389,7 +433,7 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t s
   auto kern = attn_fwd_kernel<D>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(p.nqb * a.BH);
+  const unsigned grid = (unsigned)(p.nqb2 * a.BH);
   timing_mark_start(st);
   kern<<<grid, NTHREADS, L::ALLOC, st>>>(mq, mk, mv, p);
   timing_mark_stop(st);
