@@ -7,7 +7,8 @@
 // keys j <= i on global positions (AutoSP, section 2.A item 4).
 //
 // One CTA per (head, 256-row query block) = two 128-row query tiles "a" and
-// "b" that share every K/V tile, heaviest causal blocks first.
+// "b" that share every K/V tile; CTAs run head by head (K/V reuse in L2),
+// heaviest causal blocks first within a head.
 // Warp roles (320 threads):
 //   warps 0-3  softmax of tile a, warps 4-7 softmax of tile b: thread t of
 //              a warpgroup owns query row t of its tile.  It reads its row
@@ -115,8 +116,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int blk = blockIdx.x;
-  const int qb = p.causal ? (p.nqb2 - 1 - blk / p.BH) : (blk / p.BH);
-  const int bh = blk % p.BH;
+  // Head-major order: the CTAs resident at one time cover one or two heads,
+  // whose K and V then stay in L2 for every query block that reads them;
+  // within a head the heaviest (last) causal blocks go first.
+  const int bh = blk / p.nqb2;
+  const int qb = p.causal ? (p.nqb2 - 1 - blk % p.nqb2) : (blk % p.nqb2);
   const int nkv_a = kv_tiles(p, qb, 0);
   const int nkv_b = kv_tiles(p, qb, 1);
 
@@ -288,23 +292,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int kv0 = j * BN;
       const bool diag = p.causal && (j == 2 * qb + t);
       const bool masked = diag || (kv0 + BN > p.n);
-      // pass 1: row max (32 columns at a time; diagonal and ragged tiles
-      // mask keys after the row and keys beyond n)
+      // pass 1: row max over the 128 keys (one round trip to tensor memory;
+      // diagonal and ragged tiles mask keys after the row and beyond n)
       float mx = -INFINITY;
+      {
+        uint32_t s[BN];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t s[32];
-        tmem_ld32(tS + c * 32, s);
+        for (int c = 0; c < BN / 32; ++c)
+          tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
         tmem_wait_ld();
         if (masked) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int kv = kv0 + c * 32 + k;
+          for (int k = 0; k < BN; ++k) {
+            const int kv = kv0 + k;
             if ((diag && kv > q_idx) || kv >= p.n) s[k] = __float_as_uint(-INFINITY);
           }
         }
 #pragma unroll
-        for (int k = 0; k < 32; ++k) mx = fmaxf(mx, __uint_as_float(s[k]));
+        for (int k = 0; k < BN; ++k) mx = fmaxf(mx, __uint_as_float(s[k]));
       }
       mx *= p.scale_log2;  // scale > 0: the max commutes with the scaling
       float alpha = 1.0f;
@@ -335,30 +340,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // [16k, 16k+8) (P_hi) and [16k+8, 16k+16) (P_lo), two keys per column.
       float rs = 0.0f;
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t s[32];
-        tmem_ld32(tS + c * 32, s);
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t s[64];
+        tmem_ld32(tS + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+        tmem_ld32(tS + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
         tmem_wait_ld();
         if (masked) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int kv = kv0 + c * 32 + k;
+          for (int k = 0; k < 64; ++k) {
+            const int kv = kv0 + hf * 64 + k;
             if ((diag && kv > q_idx) || kv >= p.n) s[k] = __float_as_uint(-INFINITY);
           }
         }
-        uint32_t pk[32];
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(s[k]), p.scale_log2, -mref));
-          const float p1 = ex2(fmaf(__uint_as_float(s[k + 1]), p.scale_log2, -mref));
-          rs += p0 + p1;
-          const uint32_t h = pack_bf16(p0, p1);
-          const int g = k >> 4, w = (k & 15) >> 1;  // 16-key group, pair within it
-          pk[g * 16 + w] = h;
-          pk[g * 16 + 8 + w] =
-              pack_bf16(p0 - __uint_as_float(h << 16), p1 - __uint_as_float(h & 0xffff0000u));
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            const float p0 = ex2(fmaf(__uint_as_float(s[c * 32 + k]), p.scale_log2, -mref));
+            const float p1 = ex2(fmaf(__uint_as_float(s[c * 32 + k + 1]), p.scale_log2, -mref));
+            rs += p0 + p1;
+            const uint32_t h = pack_bf16(p0, p1);
+            const int g = k >> 4, w = (k & 15) >> 1;  // 16-key group, pair within it
+            pk[g * 16 + w] = h;
+            pk[g * 16 + 8 + w] =
+                pack_bf16(p0 - __uint_as_float(h << 16), p1 - __uint_as_float(h & 0xffff0000u));
+          }
+          tmem_st32(tS + hf * 64 + c * 32, pk);
         }
-        tmem_st32(tS + c * 32, pk);
       }
       l = l * alpha + rs;
       tmem_wait_st();
