@@ -15,38 +15,43 @@
 //               tiles i that see block j (i >= j when causal);
 //   bwd_dq_cvt  dQ accumulator (fp32) -> dQ (bf16).
 //
-// bwd_main roles (192 threads):
-//   warps 0-3  compute: thread t owns key row j*128+t for S^T, dP^T, dV, dK
-//              (tensor-memory lane t) and query row i*128+t for dQ_i;
-//   warp 4     TMA producer: K_j, V_j once; Q_i (2 stages), dO_i (1 stage);
-//   warp 5     MMA issuer.  Per tile:  S^T = K_j Q_i^T,  dP^T = V_j dO_i^T,
-//              then after P^T and dS^T are in shared memory:
-//              dV += P^T dO_i,  dK += dS^T Q_i,  dQ_i = dS K_j.
-// Tensor memory: S^T [0,128), dP^T and dQ_i [128,256), dV [256,256+d),
-// dK [256+d, 256+2d).  dQ_i is added into the fp32 accumulator with
-// vector reductions (red.global.add.v4.f32).
+// bwd_main roles (448 threads):
+//   warps 0-7  compute, two warpgroups: warpgroup w takes queries
+//              [64w, 64w+64) of each tile; thread r owns key row j*128 + r
+//              (tensor-memory lane r).  P^T = exp2(S^T scale log2e - LSE)
+//              is written back as bf16 over the S^T columns it was read from
+//              and feeds dV from tensor memory; dS^T = P^T o (dP^T - D) goes
+//              to a 128-byte-swizzled shared tile read by dK (K-major) and
+//              dQ (MN-major, as dS).
+//   warps 8-11 dQ drain: reads dQ_i (lane = query row) and adds it into the
+//              fp32 accumulator with red.global.add.v4.f32 while the next
+//              tile is computed.
+//   warp 12    TMA producer: K_j, V_j once; Q_i (2 stages), dO_i (1 stage).
+//   warp 13    MMA issuer.  Per tile:  S^T = K_j Q_i^T,  dP^T = V_j dO_i^T,
+//              then  dV += P^T dO_i,  dK += dS^T Q_i,  dQ_i = dS K_j.
+// Tensor memory: S^T / P^T [0,128), dP^T and dQ_i [128,256), dV [256,256+d),
+// dK [256+d, 256+2d).  CTAs run head by head so the key blocks of a head
+// share Q, dO, LSE and D through L2.
 #include "internal.h"
 
 namespace chain {
 namespace {
 
 constexpr int BM = 128;  // rows per tile (keys and queries)
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 448;
 
 template <int D>
 struct BwdLayout {
-  static constexpr uint32_t T_BYTES = BM * D * 2;  // one [128][D] bf16 tile
-  static constexpr uint32_t S_BYTES = BM * BM * 2; // one [128][128] bf16 tile
+  static constexpr uint32_t T_BYTES = BM * D * 2;   // one [128][D] bf16 tile
+  static constexpr uint32_t S_BYTES = BM * BM * 2;  // one [128][128] bf16 tile
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + T_BYTES;
   static constexpr uint32_t OFF_Q = OFF_V + T_BYTES;       // 2 stages
   static constexpr uint32_t OFF_DO = OFF_Q + 2 * T_BYTES;  // 1 stage
-  static constexpr uint32_t OFF_PT = OFF_DO + T_BYTES;
-  static constexpr uint32_t OFF_DST = OFF_PT + S_BYTES;
-  static constexpr uint32_t OFF_LSE = OFF_DST + S_BYTES;   // 128 floats
-  static constexpr uint32_t OFF_DV = OFF_LSE + BM * 4;     // 128 floats
-  static constexpr uint32_t OFF_BAR = OFF_DV + BM * 4;
-  static constexpr uint32_t NBAR = 12;
+  static constexpr uint32_t OFF_DST = OFF_DO + T_BYTES;
+  static constexpr uint32_t OFF_LD = OFF_DST + S_BYTES;    // LSE and D staging, 2 KB
+  static constexpr uint32_t OFF_BAR = OFF_LD + 2048;
+  static constexpr uint32_t NBAR = 15;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   static constexpr uint32_t ALLOC = (BYTES + 1024 > 120 * 1024) ? BYTES + 1024 : 120 * 1024;
@@ -144,36 +149,44 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t *q_empty = bars + 3;  // [2]
   uint64_t *do_full = bars + 5;
   uint64_t *do_empty = bars + 6;
-  uint64_t *sdp_full = bars + 7;
-  uint64_t *p_ready = bars + 8;
-  uint64_t *dq_full = bars + 9;
-  uint64_t *dq_free = bars + 10;
-  uint64_t *fin = bars + 11;
+  uint64_t *s_full = bars + 7;
+  uint64_t *dp_full = bars + 8;
+  uint64_t *p_ready = bars + 9;   // both compute warpgroups (256 arrivals)
+  uint64_t *dq_full = bars + 10;
+  uint64_t *dq_free = bars + 11;  // drain warpgroup (128 arrivals)
+  uint64_t *ds_free = bars + 12;
+  uint64_t *fin = bars + 13;
+  uint64_t *mma_drain = bars + 14;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
-  uint64_t *mma_drain = reinterpret_cast<uint64_t *>(smem + L::OFF_MISC + 8);
-  float *sL = reinterpret_cast<float *>(smem + L::OFF_LSE);
-  float *sDv = reinterpret_cast<float *>(smem + L::OFF_DV);
+  // staged LSE (log2 units) and D: [warpgroup][buffer][64 queries]
+  float *sL = reinterpret_cast<float *>(smem + L::OFF_LD);
+  float *sDv = sL + 2 * 2 * 64;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int jb = blockIdx.x / p.BH;  // key block; heaviest (smallest j) first when causal
-  const int bh = blockIdx.x % p.BH;
+  // head-major order: the key blocks of one head run together and share
+  // Q, dO, LSE and D through L2; smallest (heaviest causal) block first
+  const int bh = blockIdx.x / p.nqb;
+  const int jb = blockIdx.x % p.nqb;
   const int i_begin = p.causal ? jb : 0;
   const int T = p.nqb - i_begin;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < (int)L::NBAR; ++b)
-      mbar_init(&bars[b], (&bars[b] == p_ready || &bars[b] == dq_free) ? 128u : 1u);
-    mbar_init(mma_drain, 1);
+    for (int b = 0; b < (int)L::NBAR; ++b) {
+      uint32_t cnt = 1;
+      if (&bars[b] == p_ready) cnt = 256;
+      if (&bars[b] == dq_free) cnt = 128;
+      mbar_init(&bars[b], cnt);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 13) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 12 && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -184,7 +197,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 12) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       int q_issued = 0, do_issued = 0;
@@ -220,183 +233,225 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 13) {
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0);  // S^T, dP^T
-      const uint32_t id_kv = idesc_bf16_f32(BM, D, 0, 1);  // dV, dK
+      const uint32_t id_kv = idesc_bf16_f32(BM, D, 0, 1);  // dV (A in TMEM), dK
       const uint32_t id_q = idesc_bf16_f32(BM, D, 1, 1);   // dQ
       const uint32_t sK = smem_u32(smem + L::OFF_K);
       const uint32_t sV = smem_u32(smem + L::OFF_V);
       const uint32_t sQ0 = smem_u32(smem + L::OFF_Q);
       const uint32_t sdO = smem_u32(smem + L::OFF_DO);
-      const uint32_t sPT = smem_u32(smem + L::OFF_PT);
       const uint32_t sdST = smem_u32(smem + L::OFF_DST);
       const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
-      if (mbar_wait(kv_full, 0, p.wc, abort_flag, SITE_BWD_MMA)) {
-        for (int t = 0; t < T; ++t) {
-          const int qs = t & 1;
-          const uint32_t sQ = sQ0 + qs * L::T_BYTES;
-          if (!mbar_wait(&q_full[qs], (t >> 1) & 1, p.wc, abort_flag, SITE_BWD_MMA)) break;
-          tc_fence_after();
+      auto issue_s = [&](int t) {  // S^T = K_j Q_t^T
+        const uint32_t sQ = sQ0 + (t & 1) * L::T_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-            umma_f16_ss(tS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024),
-                        id_s, kk > 0 ? 1u : 0u);
-          }
-          if (!mbar_wait(do_full, t & 1, p.wc, abort_flag, SITE_BWD_MMA)) break;
-          if (t >= 1 && !mbar_wait(dq_free, (t - 1) & 1, p.wc, abort_flag, SITE_BWD_MMA)) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-            umma_f16_ss(tdP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdO + off, 16, 1024),
-                        id_s, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(sdp_full);
-          if (!mbar_wait(p_ready, t & 1, p.wc, abort_flag, SITE_BWD_MMA)) break;
-          tc_fence_after();
-          // dV += P^T dO_i   (A: P^T K-major over queries; B: dO MN-major)
-#pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-            umma_f16_ss(tdV, sdesc_sw128(sPT + aoff, 16, 1024),
-                        sdesc_sw128(sdO + kk * 2048, BM * 128, 1024), id_kv,
-                        (t > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(do_empty);
-          // dK += dS^T Q_i
-#pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-            umma_f16_ss(tdK, sdesc_sw128(sdST + aoff, 16, 1024),
-                        sdesc_sw128(sQ + kk * 2048, BM * 128, 1024), id_kv,
-                        (t > 0 || kk > 0) ? 1u : 0u);
-          }
-          // dQ_i = dS K_j   (A: dS read MN-major from the dS^T tile; B: K MN-major)
-#pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk) {
-            umma_f16_ss(tdP, sdesc_sw128(sdST + kk * 2048, BM * 128, 1024),
-                        sdesc_sw128(sK + kk * 2048, BM * 128, 1024), id_q, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(dq_full);
-          umma_commit(&q_empty[qs]);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          umma_f16_ss(tS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), id_s,
+                      kk > 0 ? 1u : 0u);
         }
-        umma_commit(fin);
+      };
+      auto issue_dp = [&]() {  // dP^T = V_j dO_t^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          umma_f16_ss(tdP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdO + off, 16, 1024),
+                      id_s, kk > 0 ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(kv_full, 0, p.wc, abort_flag, SITE_BWD_MMA) &&
+                mbar_wait(&q_full[0], 0, p.wc, abort_flag, SITE_BWD_MMA);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        umma_commit(s_full);
+        ok = mbar_wait(do_full, 0, p.wc, abort_flag, SITE_BWD_MMA);
+        if (ok) {
+          tc_fence_after();
+          issue_dp();
+          umma_commit(dp_full);
+        }
       }
+      for (int t = 0; ok && t < T; ++t) {
+        const int qs = t & 1;
+        const uint32_t sQ = sQ0 + qs * L::T_BYTES;
+        if (!mbar_wait(p_ready, t & 1, p.wc, abort_flag, SITE_BWD_MMA)) break;
+        tc_fence_after();
+        // dV += P^T dO_t: A = P^T in tensor memory (queries [64w, 64w+64)
+        // packed into columns [64w, 64w+32)), B = dO MN-major
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          umma_f16_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8,
+                      sdesc_sw128(sdO + kk * 2048, BM * 128, 1024), id_kv,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(do_empty);
+        // dK += dS^T Q_t
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          umma_f16_ss(tdK, sdesc_sw128(sdST + aoff, 16, 1024),
+                      sdesc_sw128(sQ + kk * 2048, BM * 128, 1024), id_kv,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        // dQ_t = dS K_j (A: dS read MN-major from the dS^T tile; B: K MN-major)
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          umma_f16_ss(tdP, sdesc_sw128(sdST + kk * 2048, BM * 128, 1024),
+                      sdesc_sw128(sK + kk * 2048, BM * 128, 1024), id_q, kk > 0 ? 1u : 0u);
+        umma_commit(dq_full);
+        umma_commit(&q_empty[qs]);
+        umma_commit(ds_free);
+        if (t + 1 < T) {
+          if (!mbar_wait(&q_full[(t + 1) & 1], ((t + 1) >> 1) & 1, p.wc, abort_flag, SITE_BWD_MMA))
+            break;
+          tc_fence_after();
+          issue_s(t + 1);  // after dV_t in issue order: P^T_t is consumed first
+          umma_commit(s_full);
+          if (!mbar_wait(do_full, (t + 1) & 1, p.wc, abort_flag, SITE_BWD_MMA)) break;
+          if (!mbar_wait(dq_free, t & 1, p.wc, abort_flag, SITE_BWD_MMA)) break;
+          tc_fence_after();
+          issue_dp();
+          umma_commit(dp_full);
+        }
+      }
+      if (ok) umma_commit(fin);
       umma_commit(mma_drain);
       drain_wait(mma_drain, 0, p.wc);
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------------------ compute
-    const int tid = threadIdx.x;  // 0..127
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const int kv_idx = jb * BM + tid;
-    const bool kv_ok = kv_idx < p.n;
-    const uint32_t sPT = smem_u32(smem + L::OFF_PT);
-    const uint32_t sdST = smem_u32(smem + L::OFF_DST);
-    bool ok = true;
-    for (int t = 0; t < T && ok; ++t) {
-      const int i = i_begin + t;
-      const bool diag = p.causal && (i == jb);
-      // stage LSE (log2 units) and D of the 128 queries of tile i
-      named_bar_sync(1, 128);
-      {
-        const int q = i * BM + tid;
-        const bool q_ok = q < p.n;
-        sL[tid] = q_ok ? p.LSE[(int64_t)bh * p.n + q] * 1.4426950408889634f : INFINITY;
-        sDv[tid] = q_ok ? p.Dvec[(int64_t)bh * p.n + q] : 0.0f;
-      }
-      named_bar_sync(1, 128);
-      if (!mbar_wait(sdp_full, t & 1, p.wc, abort_flag, SITE_BWD_COMPUTE)) {
-        ok = false;
-        break;
-      }
+  } else if (warp >= 8) {
+    // ----------------------------------------------------- dQ drain (WG2)
+    const int r = threadIdx.x - 256;  // tensor-memory lane = query row of dQ_t
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    for (int t = 0; t < T; ++t) {
+      if (!mbar_wait(dq_full, t & 1, p.wc, abort_flag, SITE_BWD_DRAIN + 0x10)) break;
       tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < BM / 32; ++c) {
-        uint32_t s[32], dp[32];
-        tmem_ld32(tmem + lane_off + c * 32, s);
-        tmem_ld32(tmem + lane_off + 128 + c * 32, dp);
-        tmem_wait_ld();
-        uint32_t pp[16], dd[16];
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int qq = c * 32 + k + u;
-            float pr = ex2(fmaf(__uint_as_float(s[k + u]), p.scale_log2, -sL[qq]));
-            if (!kv_ok || (diag && i * BM + qq < kv_idx)) pr = 0.0f;
-            pv[u] = pr;
-            dv[u] = pr * (__uint_as_float(dp[k + u]) - sDv[qq]);
-          }
-          pp[k / 2] = pack_bf16(pv[0], pv[1]);
-          dd[k / 2] = pack_bf16(dv[0], dv[1]);
-        }
-        // queries [32c, 32c+32) = chunks 4(c%2)..4(c%2)+3 of half c/2
-        const uint32_t hoff = (c >> 1) * (BM * 128);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t off = hoff + sw128_off(tid, (c & 1) * 4 + u);
-          st_shared_v4(sPT + off, pp[4 * u], pp[4 * u + 1], pp[4 * u + 2], pp[4 * u + 3]);
-          st_shared_v4(sdST + off, dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(p_ready);
-      // dQ_i: tensor-memory lane tid holds query row i*128 + tid.
-      if (!mbar_wait(dq_full, t & 1, p.wc, abort_flag, SITE_BWD_COMPUTE)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int q = i * BM + tid;
+      const int q = (i_begin + t) * BM + r;
       float *dst = p.dq_acc + ((int64_t)bh * p.n + q) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + 128 + c * 32, r);
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + 128 + c * 32, v);
         tmem_wait_ld();
         if (q < p.n) {
 #pragma unroll
           for (int k = 0; k < 32; k += 4)
-            red_add_v4(dst + c * 32 + k, __uint_as_float(r[k]) * p.scale,
-                       __uint_as_float(r[k + 1]) * p.scale, __uint_as_float(r[k + 2]) * p.scale,
-                       __uint_as_float(r[k + 3]) * p.scale);
+            red_add_v4(dst + c * 32 + k, __uint_as_float(v[k]) * p.scale,
+                       __uint_as_float(v[k + 1]) * p.scale, __uint_as_float(v[k + 2]) * p.scale,
+                       __uint_as_float(v[k + 3]) * p.scale);
         }
       }
       tc_fence_before();
       mbar_arrive(dq_free);
     }
+  } else {
+    // ------------------------------------------- compute (WG0 and WG1)
+    // Warpgroup w handles queries [64w, 64w+64) of every tile; thread r
+    // owns key row j*128 + r (tensor-memory lane r).
+    const int w = warp >> 2;
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int kv_idx = jb * BM + r;
+    const bool kv_ok = kv_idx < p.n;
+    const uint32_t sdST = smem_u32(smem + L::OFF_DST);
+    bool ok = true;
+    for (int t = 0; t < T && ok; ++t) {
+      const int i = i_begin + t, buf = t & 1;
+      const bool diag = p.causal && (i == jb);
+      float *wl = sL + (w * 2 + buf) * 64;
+      float *wd = sDv + (w * 2 + buf) * 64;
+      if (r < 64) {
+        const int q = i * BM + 64 * w + r;
+        const bool q_ok = q < p.n;
+        wl[r] = q_ok ? p.LSE[(int64_t)bh * p.n + q] * 1.4426950408889634f : INFINITY;
+        wd[r] = q_ok ? p.Dvec[(int64_t)bh * p.n + q] : 0.0f;
+      }
+      named_bar_sync(1 + w, 128);
+      if (!mbar_wait(s_full, t & 1, p.wc, abort_flag, SITE_BWD_COMPUTE)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // P^T for the 64 queries: packed bf16 pairs, written over the S^T
+      // columns this warpgroup has just read
+      uint32_t pk[32];
+      {
+        uint32_t sv[64];
+        tmem_ld32(tmem + lane_off + 64 * w, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(tmem + lane_off + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          float pv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int qq = c + u;
+            float pr = ex2(fmaf(__uint_as_float(sv[qq]), p.scale_log2, -wl[qq]));
+            if (!kv_ok || (diag && 64 * w + qq < r)) pr = 0.0f;
+            pv[u] = pr;
+          }
+          pk[c / 2] = pack_bf16(pv[0], pv[1]);
+        }
+      }
+      tmem_st32(tmem + lane_off + 64 * w, pk);
+      if (!mbar_wait(dp_full, t & 1, p.wc, abort_flag, SITE_BWD_COMPUTE)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (t >= 1 && !mbar_wait(ds_free, (t - 1) & 1, p.wc, abort_flag, SITE_BWD_COMPUTE)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t dp[32];
+        tmem_ld32(tmem + lane_off + 128 + 64 * w + 32 * h, dp);
+        tmem_wait_ld();
+        uint32_t dd[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const int qq = 32 * h + k;
+          const uint32_t pp = pk[qq / 2];
+          const float p0 = __uint_as_float(pp << 16), p1 = __uint_as_float(pp & 0xffff0000u);
+          dd[k / 2] = pack_bf16(p0 * (__uint_as_float(dp[k]) - wd[qq]),
+                                p1 * (__uint_as_float(dp[k + 1]) - wd[qq + 1]));
+        }
+        // queries [64w + 32h, +32) = chunks 4h..4h+3 of half w of the dS^T tile
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          st_shared_v4(sdST + w * (BM * 128) + sw128_off(r, 4 * h + u), dd[4 * u], dd[4 * u + 1],
+                       dd[4 * u + 2], dd[4 * u + 3]);
+      }
+      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+    }
     // --------------------------------------------------- dK, dV epilogue
     if (ok && T > 0 && mbar_wait(fin, 0, p.wc, abort_flag, SITE_BWD_EPI)) {
       tc_fence_after();
-      __nv_bfloat16 *dv_row = p.dV + ((int64_t)bh * p.n + kv_idx) * D;
-      __nv_bfloat16 *dk_row = p.dK + ((int64_t)bh * p.n + kv_idx) * D;
+      // WG0 writes dV, WG1 writes dK (times scale)
+      const uint32_t col = 256 + w * D;
+      const float mul = w ? p.scale : 1.0f;
+      __nv_bfloat16 *row = (w ? p.dK : p.dV) + ((int64_t)bh * p.n + kv_idx) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t a[32], b[32];
-        tmem_ld32(tmem + lane_off + 256 + c * 32, a);
-        tmem_ld32(tmem + lane_off + 256 + D + c * 32, b);
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_off + col + c * 32, a);
         tmem_wait_ld();
         if (kv_ok) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            uint4 va, vb;
-            va.x = pack_bf16(__uint_as_float(a[8 * k + 0]), __uint_as_float(a[8 * k + 1]));
-            va.y = pack_bf16(__uint_as_float(a[8 * k + 2]), __uint_as_float(a[8 * k + 3]));
-            va.z = pack_bf16(__uint_as_float(a[8 * k + 4]), __uint_as_float(a[8 * k + 5]));
-            va.w = pack_bf16(__uint_as_float(a[8 * k + 6]), __uint_as_float(a[8 * k + 7]));
-            vb.x = pack_bf16(__uint_as_float(b[8 * k + 0]) * p.scale, __uint_as_float(b[8 * k + 1]) * p.scale);
-            vb.y = pack_bf16(__uint_as_float(b[8 * k + 2]) * p.scale, __uint_as_float(b[8 * k + 3]) * p.scale);
-            vb.z = pack_bf16(__uint_as_float(b[8 * k + 4]) * p.scale, __uint_as_float(b[8 * k + 5]) * p.scale);
-            vb.w = pack_bf16(__uint_as_float(b[8 * k + 6]) * p.scale, __uint_as_float(b[8 * k + 7]) * p.scale);
-            reinterpret_cast<uint4 *>(dv_row + c * 32)[k] = va;
-            reinterpret_cast<uint4 *>(dk_row + c * 32)[k] = vb;
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(a[8 * k + 0]) * mul, __uint_as_float(a[8 * k + 1]) * mul);
+            v.y = pack_bf16(__uint_as_float(a[8 * k + 2]) * mul, __uint_as_float(a[8 * k + 3]) * mul);
+            v.z = pack_bf16(__uint_as_float(a[8 * k + 4]) * mul, __uint_as_float(a[8 * k + 5]) * mul);
+            v.w = pack_bf16(__uint_as_float(a[8 * k + 6]) * mul, __uint_as_float(a[8 * k + 7]) * mul);
+            reinterpret_cast<uint4 *>(row + c * 32)[k] = v;
           }
         }
       }
@@ -405,7 +460,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
