@@ -9,61 +9,70 @@
 // S = scale Q K^T, dP = dO V^T, D_i = sum_e dO_ie O_ie:
 //   dV = P^T dO,  dS = P o (dP - D),  dK = scale dS^T Q,  dQ = scale dS K.
 //
-// Three kernels:
-//   bwd_prep    D_i = sum_e dO_ie O_ie (fp32), zeroes the fp32 dQ accumulator;
-//   bwd_main    one CTA per (head, 128-key block j), looping over the query
-//               tiles i that see block j (i >= j when causal);
-//   bwd_dq_cvt  dQ accumulator (fp32) -> dQ (bf16).
+// Three kernels, no atomics, deterministic:
+//   bwd_prep   D_i = sum_e dO_ie O_ie (fp32), into the workspace;
+//   bwd_dkdv   one CTA per (head, 128-key block j), looping over the query
+//              tiles i that see block j (i >= j when causal):
+//                S^T = K_j Q_i^T,  dP^T = V_j dO_i^T      (tensor memory)
+//                P^T, dS^T written back as bf16 over those columns
+//                dV += P^T dO_i,  dK += dS^T Q_i           (A from tensor memory)
+//   bwd_dq     one CTA per (head, 128-query tile i), looping over the key
+//              tiles j <= i:
+//                S = Q_i K_j^T (two buffers),  dP = dO_i V_j^T
+//                dS written back as bf16 over the S columns
+//                dQ += dS K_j                               (A from tensor memory)
+// bwd_dq recomputes S and dP, 7 products per tile pair instead of 5, in
+// exchange for accumulating dQ on chip instead of adding 128 x 128 fp32
+// partials per tile pair into global memory.
 //
-// bwd_main roles (448 threads):
-//   warps 0-7  compute, two warpgroups: warpgroup w takes queries
-//              [64w, 64w+64) of each tile; thread r owns key row j*128 + r
-//              (tensor-memory lane r).  P^T = exp2(S^T scale log2e - LSE)
-//              is written back as bf16 over the S^T columns it was read from
-//              and feeds dV from tensor memory; dS^T = P^T o (dP^T - D) goes
-//              to a 128-byte-swizzled shared tile read by dK (K-major) and
-//              dQ (MN-major, as dS).
-//   warps 8-11 dQ drain: reads dQ_i (lane = query row) and adds it into the
-//              fp32 accumulator with red.global.add.v4.f32 while the next
-//              tile is computed.
-//   warp 12    TMA producer: K_j, V_j once; Q_i (2 stages), dO_i (1 stage).
-//   warp 13    MMA issuer.  Per tile:  S^T = K_j Q_i^T,  dP^T = V_j dO_i^T,
-//              then  dV += P^T dO_i,  dK += dS^T Q_i,  dQ_i = dS K_j.
-// Tensor memory: S^T / P^T [0,128), dP^T and dQ_i [128,256), dV [256,256+d),
-// dK [256+d, 256+2d).  CTAs run head by head so the key blocks of a head
-// share Q, dO, LSE and D through L2.
+// Roles (320 threads) in both main kernels: warps 0-7 compute, two
+// warpgroups splitting the 128 columns of each tile (warpgroup w takes
+// columns [64w, 64w+64); thread r owns row r = tensor-memory lane r); warp 8
+// TMA producer; warp 9 MMA issuer.  A warpgroup writes the bf16 result of a
+// 64-column half into the first 32 columns of that half, which it alone has
+// read, so the two warpgroups never overwrite each other's inputs.  The
+// MMAs of one thread execute in issue order, so an MMA that overwrites a
+// tensor-memory region is issued after the MMAs that read it, and its
+// completion tells the compute warps the old contents are consumed.
 #include "internal.h"
 
 namespace chain {
 namespace {
 
 constexpr int BM = 128;  // rows per tile (keys and queries)
-constexpr int NTHREADS = 448;
+constexpr int NTHREADS = 320;
 
 template <int D>
 struct BwdLayout {
-  static constexpr uint32_t T_BYTES = BM * D * 2;   // one [128][D] bf16 tile
-  static constexpr uint32_t S_BYTES = BM * BM * 2;  // one [128][128] bf16 tile
-  static constexpr uint32_t OFF_K = 0;
-  static constexpr uint32_t OFF_V = OFF_K + T_BYTES;
-  static constexpr uint32_t OFF_Q = OFF_V + T_BYTES;       // 2 stages
-  static constexpr uint32_t OFF_DO = OFF_Q + 2 * T_BYTES;  // 1 stage
-  static constexpr uint32_t OFF_DST = OFF_DO + T_BYTES;
-  static constexpr uint32_t OFF_LD = OFF_DST + S_BYTES;    // LSE and D staging, 2 KB
-  static constexpr uint32_t OFF_BAR = OFF_LD + 2048;
-  static constexpr uint32_t NBAR = 15;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t BYTES = OFF_MISC + 16;
-  static constexpr uint32_t ALLOC = (BYTES + 1024 > 120 * 1024) ? BYTES + 1024 : 120 * 1024;
+  static constexpr uint32_t T_BYTES = BM * D * 2;  // one [128][D] bf16 tile
+  // bwd_dkdv: K_j, V_j, Q (2 stages), dO (2 stages)
+  static constexpr uint32_t A_K = 0;
+  static constexpr uint32_t A_V = A_K + T_BYTES;
+  static constexpr uint32_t A_Q = A_V + T_BYTES;
+  static constexpr uint32_t A_DO = A_Q + 2 * T_BYTES;
+  static constexpr uint32_t A_LD = A_DO + 2 * T_BYTES;  // LSE/D staging [2 wg][2 buf][64] x2
+  static constexpr uint32_t A_BAR = A_LD + 2048;
+  // bwd_dq: Q_i, dO_i once; K, V (2 stages each)
+  static constexpr uint32_t B_Q = 0;
+  static constexpr uint32_t B_DO = B_Q + T_BYTES;
+  static constexpr uint32_t B_K = B_DO + T_BYTES;
+  static constexpr uint32_t B_V = B_K + 2 * T_BYTES;
+  static constexpr uint32_t B_BAR = B_V + 2 * T_BYTES;
+  static constexpr uint32_t NBAR = 16;
+  static constexpr uint32_t A_MISC = A_BAR + NBAR * 8;
+  static constexpr uint32_t B_MISC = B_BAR + NBAR * 8;
+  static constexpr uint32_t A_ALLOC =
+      (A_MISC + 16 + 1024 > 120 * 1024) ? A_MISC + 16 + 1024 : 120 * 1024;
+  static constexpr uint32_t B_ALLOC =
+      (B_MISC + 16 + 1024 > 120 * 1024) ? B_MISC + 16 + 1024 : 120 * 1024;
 };
 
 struct BwdParams {
-  int BH, n, nqb, causal;
+  int BH, n, nb, causal;
   float scale, scale_log2;
-  const float *LSE;  // [BH][n]
-  const float *Dvec; // [BH][n]
-  float *dq_acc;     // [BH][n][D]
-  __nv_bfloat16 *dK, *dV;
+  const float *LSE;   // [BH][n]
+  const float *Dvec;  // [BH][n]
+  __nv_bfloat16 *dQ, *dK, *dV;
   WaitCfg wc;
 };
 
@@ -72,7 +81,11 @@ enum : int {
   SITE_BWD_MMA = 0x202,
   SITE_BWD_COMPUTE = 0x203,
   SITE_BWD_EPI = 0x204,
-  SITE_BWD_DRAIN = 0x205
+  SITE_BWD_DRAIN = 0x205,
+  SITE_DQ_PROD = 0x211,
+  SITE_DQ_MMA = 0x212,
+  SITE_DQ_COMPUTE = 0x213,
+  SITE_DQ_EPI = 0x214
 };
 
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const WaitCfg &wc) {
@@ -80,15 +93,42 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const
   mbar_wait(bar, parity, wc, &never, SITE_BWD_DRAIN);
 }
 
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+  return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) &
+                                     ~static_cast<uintptr_t>(1023));
+}
+
+// NC fp32 accumulators of one row (tensor-memory columns from taddr) ->
+// bf16 row in global memory, times mul.
+template <int NC>
+__device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16 *row, float mul,
+                                               bool ok) {
+#pragma unroll 1
+  for (int c = 0; c < NC / 32; ++c) {
+    uint32_t a[32];
+    tmem_ld32(taddr + c * 32, a);
+    tmem_wait_ld();
+    if (ok) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint4 v;
+        v.x = pack_bf16(__uint_as_float(a[8 * k + 0]) * mul, __uint_as_float(a[8 * k + 1]) * mul);
+        v.y = pack_bf16(__uint_as_float(a[8 * k + 2]) * mul, __uint_as_float(a[8 * k + 3]) * mul);
+        v.z = pack_bf16(__uint_as_float(a[8 * k + 4]) * mul, __uint_as_float(a[8 * k + 5]) * mul);
+        v.w = pack_bf16(__uint_as_float(a[8 * k + 6]) * mul, __uint_as_float(a[8 * k + 7]) * mul);
+        reinterpret_cast<uint4 *>(row + c * 32)[k] = v;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------ preprocess
 // 16 threads per row of d = 128 (8 per row of d = 64): each loads 16 bytes
-// of O and dO, the partial dot products are reduced with shuffles.
+// of O and dO; the partial dot products are reduced with shuffles.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__restrict__ O,
                                                        const __nv_bfloat16 *__restrict__ dO,
-                                                       float *__restrict__ Dvec,
-                                                       float *__restrict__ dq_acc,
-                                                       int64_t rows) {
+                                                       float *__restrict__ Dvec, int64_t rows) {
   constexpr int TPR = D / 8;  // threads per row
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t row = tid / TPR;
@@ -106,87 +146,57 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
       acc = fmaf(fa.x, fb.x, acc);
       acc = fmaf(fa.y, fb.y, acc);
     }
-    float4 *z = reinterpret_cast<float4 *>(dq_acc + row * D + part * 8);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (row < rows && part == 0) Dvec[row] = acc;
 }
 
-// ------------------------------------------------------------ dQ convert
-__global__ void __launch_bounds__(256) bwd_dq_cvt_kernel(const float *__restrict__ acc,
-                                                         __nv_bfloat16 *__restrict__ dq,
-                                                         int64_t n8) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4 *>(acc)[2 * i];
-    const float4 b = reinterpret_cast<const float4 *>(acc)[2 * i + 1];
-    uint4 o;
-    o.x = pack_bf16(a.x, a.y);
-    o.y = pack_bf16(a.z, a.w);
-    o.z = pack_bf16(b.x, b.y);
-    o.w = pack_bf16(b.z, b.w);
-    reinterpret_cast<uint4 *>(dq)[i] = o;
-  }
-}
-
-// ------------------------------------------------------------ main kernel
+// ------------------------------------------------------- dK, dV kernel
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmdO, const BwdParams p) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+  uint8_t *smem = align1024(smem_raw);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::A_BAR);
   uint64_t *kv_full = bars + 0;
-  uint64_t *q_full = bars + 1;   // [2]
-  uint64_t *q_empty = bars + 3;  // [2]
-  uint64_t *do_full = bars + 5;
-  uint64_t *do_empty = bars + 6;
-  uint64_t *s_full = bars + 7;
-  uint64_t *dp_full = bars + 8;
-  uint64_t *p_ready = bars + 9;   // both compute warpgroups (256 arrivals)
-  uint64_t *dq_full = bars + 10;
-  uint64_t *dq_free = bars + 11;  // drain warpgroup (128 arrivals)
-  uint64_t *ds_free = bars + 12;
-  uint64_t *fin = bars + 13;
-  uint64_t *mma_drain = bars + 14;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
-  // staged LSE (log2 units) and D: [warpgroup][buffer][64 queries]
-  float *sL = reinterpret_cast<float *>(smem + L::OFF_LD);
-  float *sDv = sL + 2 * 2 * 64;
+  uint64_t *q_full = bars + 1;    // [2]
+  uint64_t *q_empty = bars + 3;   // [2]
+  uint64_t *do_full = bars + 5;   // [2]
+  uint64_t *do_empty = bars + 7;  // [2]
+  uint64_t *s_full = bars + 9;
+  uint64_t *dp_full = bars + 10;
+  uint64_t *p_ready = bars + 11;  // both compute warpgroups (256 arrivals)
+  uint64_t *fin = bars + 12;
+  uint64_t *mma_drain = bars + 13;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::A_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::A_MISC + 4);
+  float *sL = reinterpret_cast<float *>(smem + L::A_LD);  // [wg][buf][64], LSE in log2 units
+  float *sDv = sL + 2 * 2 * 64;                            // [wg][buf][64]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // head-major order: the key blocks of one head run together and share
-  // Q, dO, LSE and D through L2; smallest (heaviest causal) block first
-  const int bh = blockIdx.x / p.nqb;
-  const int jb = blockIdx.x % p.nqb;
+  // head-major order: the key blocks of one head run together and share Q,
+  // dO, LSE and D through L2; smallest (heaviest causal) block first
+  const int bh = blockIdx.x / p.nb;
+  const int jb = blockIdx.x % p.nb;
   const int i_begin = p.causal ? jb : 0;
-  const int T = p.nqb - i_begin;
+  const int T = p.nb - i_begin;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < (int)L::NBAR; ++b) {
-      uint32_t cnt = 1;
-      if (&bars[b] == p_ready) cnt = 256;
-      if (&bars[b] == dq_free) cnt = 128;
-      mbar_init(&bars[b], cnt);
-    }
+    for (int b = 0; b < 14; ++b) mbar_init(&bars[b], &bars[b] == p_ready ? 256u : 1u);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 13) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  if (warp == 12 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -196,125 +206,103 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
 
-  if (warp == 12) {
+  if (warp == 8) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       int q_issued = 0, do_issued = 0;
       mbar_arrive_expect_tx(kv_full, 2 * L::T_BYTES);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(smem + L::OFF_K + c * (BM * 128), &tmK, kv_full, c * 64, jb * BM, bh);
-        tma_load_3d(smem + L::OFF_V + c * (BM * 128), &tmV, kv_full, c * 64, jb * BM, bh);
+        tma_load_3d(smem + L::A_K + c * (BM * 128), &tmK, kv_full, c * 64, jb * BM, bh);
+        tma_load_3d(smem + L::A_V + c * (BM * 128), &tmV, kv_full, c * 64, jb * BM, bh);
       }
       for (int t = 0; t < T; ++t) {
-        const int i = i_begin + t, qs = t & 1;
-        if (t >= 2 &&
-            !mbar_wait(&q_empty[qs], ((t >> 1) - 1) & 1, p.wc, abort_flag, SITE_BWD_PROD))
+        const int i = i_begin + t, s = t & 1;
+        if (t >= 2 && !mbar_wait(&q_empty[s], ((t >> 1) - 1) & 1, p.wc, abort_flag, SITE_BWD_PROD))
           break;
-        mbar_arrive_expect_tx(&q_full[qs], L::T_BYTES);
+        mbar_arrive_expect_tx(&q_full[s], L::T_BYTES);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + L::OFF_Q + qs * L::T_BYTES + c * (BM * 128), &tmQ, &q_full[qs],
-                      c * 64, i * BM, bh);
+          tma_load_3d(smem + L::A_Q + s * L::T_BYTES + c * (BM * 128), &tmQ, &q_full[s], c * 64,
+                      i * BM, bh);
         q_issued = t + 1;
-        if (t >= 1 && !mbar_wait(do_empty, (t - 1) & 1, p.wc, abort_flag, SITE_BWD_PROD)) break;
-        mbar_arrive_expect_tx(do_full, L::T_BYTES);
+        if (t >= 2 && !mbar_wait(&do_empty[s], ((t >> 1) - 1) & 1, p.wc, abort_flag, SITE_BWD_PROD))
+          break;
+        mbar_arrive_expect_tx(&do_full[s], L::T_BYTES);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + L::OFF_DO + c * (BM * 128), &tmdO, do_full, c * 64, i * BM, bh);
+          tma_load_3d(smem + L::A_DO + s * L::T_BYTES + c * (BM * 128), &tmdO, &do_full[s], c * 64,
+                      i * BM, bh);
         do_issued = t + 1;
       }
       if (*abort_flag) {
         drain_wait(kv_full, 0, p.wc);
         for (int t = (q_issued > 2 ? q_issued - 2 : 0); t < q_issued; ++t)
           drain_wait(&q_full[t & 1], (t >> 1) & 1, p.wc);
-        if (do_issued > 0) drain_wait(do_full, (do_issued - 1) & 1, p.wc);
+        for (int t = (do_issued > 2 ? do_issued - 2 : 0); t < do_issued; ++t)
+          drain_wait(&do_full[t & 1], (t >> 1) & 1, p.wc);
       }
     }
     __syncwarp();
-  } else if (warp == 13) {
+  } else if (warp == 9) {
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0);  // S^T, dP^T
-      const uint32_t id_kv = idesc_bf16_f32(BM, D, 0, 1);  // dV (A in TMEM), dK
-      const uint32_t id_q = idesc_bf16_f32(BM, D, 1, 1);   // dQ
-      const uint32_t sK = smem_u32(smem + L::OFF_K);
-      const uint32_t sV = smem_u32(smem + L::OFF_V);
-      const uint32_t sQ0 = smem_u32(smem + L::OFF_Q);
-      const uint32_t sdO = smem_u32(smem + L::OFF_DO);
-      const uint32_t sdST = smem_u32(smem + L::OFF_DST);
-      const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
-      auto issue_s = [&](int t) {  // S^T = K_j Q_t^T
-        const uint32_t sQ = sQ0 + (t & 1) * L::T_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          umma_f16_ss(tS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), id_s,
-                      kk > 0 ? 1u : 0u);
-        }
-      };
-      auto issue_dp = [&]() {  // dP^T = V_j dO_t^T
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          umma_f16_ss(tdP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdO + off, 16, 1024),
-                      id_s, kk > 0 ? 1u : 0u);
-        }
-      };
-      bool ok = mbar_wait(kv_full, 0, p.wc, abort_flag, SITE_BWD_MMA) &&
-                mbar_wait(&q_full[0], 0, p.wc, abort_flag, SITE_BWD_MMA);
-      if (ok) {
+      const uint32_t id_kv = idesc_bf16_f32(BM, D, 0, 1);  // dV, dK (A in tensor memory)
+      const uint32_t sK = smem_u32(smem + L::A_K);
+      const uint32_t sV = smem_u32(smem + L::A_V);
+      const uint32_t sQ0 = smem_u32(smem + L::A_Q);
+      const uint32_t sdO0 = smem_u32(smem + L::A_DO);
+      auto issue_sdp = [&](int t) -> bool {
+        const int s = t & 1;
+        if (!mbar_wait(&q_full[s], (t >> 1) & 1, p.wc, abort_flag, SITE_BWD_MMA)) return false;
         tc_fence_after();
-        issue_s(0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K_j Q_t^T
+          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          umma_f16_ss(tS, sdesc_sw128(sK + off, 16, 1024),
+                      sdesc_sw128(sQ0 + s * L::T_BYTES + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+        }
         umma_commit(s_full);
-        ok = mbar_wait(do_full, 0, p.wc, abort_flag, SITE_BWD_MMA);
-        if (ok) {
-          tc_fence_after();
-          issue_dp();
-          umma_commit(dp_full);
-        }
-      }
-      for (int t = 0; ok && t < T; ++t) {
-        const int qs = t & 1;
-        const uint32_t sQ = sQ0 + qs * L::T_BYTES;
-        if (!mbar_wait(p_ready, t & 1, p.wc, abort_flag, SITE_BWD_MMA)) break;
+        if (!mbar_wait(&do_full[s], (t >> 1) & 1, p.wc, abort_flag, SITE_BWD_MMA)) return false;
         tc_fence_after();
-        // dV += P^T dO_t: A = P^T in tensor memory (queries [64w, 64w+64)
-        // packed into columns [64w, 64w+32)), B = dO MN-major
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          umma_f16_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8,
-                      sdesc_sw128(sdO + kk * 2048, BM * 128, 1024), id_kv,
-                      (t > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(do_empty);
-        // dK += dS^T Q_t
-#pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          umma_f16_ss(tdK, sdesc_sw128(sdST + aoff, 16, 1024),
-                      sdesc_sw128(sQ + kk * 2048, BM * 128, 1024), id_kv,
-                      (t > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V_j dO_t^T
+          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          umma_f16_ss(tdP, sdesc_sw128(sV + off, 16, 1024),
+                      sdesc_sw128(sdO0 + s * L::T_BYTES + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
-        // dQ_t = dS K_j (A: dS read MN-major from the dS^T tile; B: K MN-major)
+        umma_commit(dp_full);
+        return true;
+      };
+      bool ok = mbar_wait(kv_full, 0, p.wc, abort_flag, SITE_BWD_MMA) && (T == 0 || issue_sdp(0));
+      for (int t = 0; ok && t < T; ++t) {
+        const int s = t & 1;
+        if (!mbar_wait(p_ready, t & 1, p.wc, abort_flag, SITE_BWD_MMA)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // A operands from tensor memory: queries [64w, 64w+64) of P^T (dS^T)
+        // sit packed in columns [64w, 64w+32) of the S^T (dP^T) region.
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          umma_f16_ss(tdP, sdesc_sw128(sdST + kk * 2048, BM * 128, 1024),
-                      sdesc_sw128(sK + kk * 2048, BM * 128, 1024), id_q, kk > 0 ? 1u : 0u);
-        umma_commit(dq_full);
-        umma_commit(&q_empty[qs]);
-        umma_commit(ds_free);
-        if (t + 1 < T) {
-          if (!mbar_wait(&q_full[(t + 1) & 1], ((t + 1) >> 1) & 1, p.wc, abort_flag, SITE_BWD_MMA))
-            break;
-          tc_fence_after();
-          issue_s(t + 1);  // after dV_t in issue order: P^T_t is consumed first
-          umma_commit(s_full);
-          if (!mbar_wait(do_full, (t + 1) & 1, p.wc, abort_flag, SITE_BWD_MMA)) break;
-          if (!mbar_wait(dq_free, t & 1, p.wc, abort_flag, SITE_BWD_MMA)) break;
-          tc_fence_after();
-          issue_dp();
-          umma_commit(dp_full);
+        for (int kk = 0; kk < BM / 16; ++kk)  // dV += P^T dO_t
+          umma_f16_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8,
+                      sdesc_sw128(sdO0 + s * L::T_BYTES + kk * 2048, BM * 128, 1024), id_kv,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&do_empty[s]);
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)  // dK += dS^T Q_t
+          umma_f16_ts(tdK, tdP + (kk >> 2) * 64 + (kk & 3) * 8,
+                      sdesc_sw128(sQ0 + s * L::T_BYTES + kk * 2048, BM * 128, 1024), id_kv,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&q_empty[s]);
+        // next tile: S^T and dP^T overwrite the regions just read, after them
+        if (t + 1 < T && !issue_sdp(t + 1)) {
+          ok = false;
+          break;
         }
       }
       if (ok) umma_commit(fin);
@@ -322,41 +310,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       drain_wait(mma_drain, 0, p.wc);
     }
     __syncwarp();
-  } else if (warp >= 8) {
-    // ----------------------------------------------------- dQ drain (WG2)
-    const int r = threadIdx.x - 256;  // tensor-memory lane = query row of dQ_t
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    for (int t = 0; t < T; ++t) {
-      if (!mbar_wait(dq_full, t & 1, p.wc, abort_flag, SITE_BWD_DRAIN + 0x10)) break;
-      tc_fence_after();
-      const int q = (i_begin + t) * BM + r;
-      float *dst = p.dq_acc + ((int64_t)bh * p.n + q) * D;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + 128 + c * 32, v);
-        tmem_wait_ld();
-        if (q < p.n) {
-#pragma unroll
-          for (int k = 0; k < 32; k += 4)
-            red_add_v4(dst + c * 32 + k, __uint_as_float(v[k]) * p.scale,
-                       __uint_as_float(v[k + 1]) * p.scale, __uint_as_float(v[k + 2]) * p.scale,
-                       __uint_as_float(v[k + 3]) * p.scale);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(dq_free);
-    }
   } else {
-    // ------------------------------------------- compute (WG0 and WG1)
-    // Warpgroup w handles queries [64w, 64w+64) of every tile; thread r
-    // owns key row j*128 + r (tensor-memory lane r).
+    // --------------------------------------------- compute (two warpgroups)
     const int w = warp >> 2;
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int kv_idx = jb * BM + r;
     const bool kv_ok = kv_idx < p.n;
-    const uint32_t sdST = smem_u32(smem + L::OFF_DST);
+    // LSE (log2 units) and D of query 64w + r of a tile (r < 64), fetched
+    // one tile ahead
+    auto fetch = [&](int i, float &lv, float &dv) {
+      const int q = i * BM + 64 * w + r;
+      const bool q_ok = r < 64 && q < p.n;
+      lv = q_ok ? __ldg(p.LSE + (int64_t)bh * p.n + q) * 1.4426950408889634f : INFINITY;
+      dv = q_ok ? __ldg(p.Dvec + (int64_t)bh * p.n + q) : 0.0f;
+    };
+    float l_next = INFINITY, d_next = 0.0f;
+    if (T > 0) fetch(i_begin, l_next, d_next);
     bool ok = true;
     for (int t = 0; t < T && ok; ++t) {
       const int i = i_begin + t, buf = t & 1;
@@ -364,69 +334,52 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       float *wl = sL + (w * 2 + buf) * 64;
       float *wd = sDv + (w * 2 + buf) * 64;
       if (r < 64) {
-        const int q = i * BM + 64 * w + r;
-        const bool q_ok = q < p.n;
-        wl[r] = q_ok ? p.LSE[(int64_t)bh * p.n + q] * 1.4426950408889634f : INFINITY;
-        wd[r] = q_ok ? p.Dvec[(int64_t)bh * p.n + q] : 0.0f;
+        wl[r] = l_next;
+        wd[r] = d_next;
       }
+      if (t + 1 < T) fetch(i + 1, l_next, d_next);
       named_bar_sync(1 + w, 128);
       if (!mbar_wait(s_full, t & 1, p.wc, abort_flag, SITE_BWD_COMPUTE)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // P^T for the 64 queries: packed bf16 pairs, written over the S^T
-      // columns this warpgroup has just read
-      uint32_t pk[32];
+      // P^T for queries [64w, 64w+64): bf16 pairs over the columns just read
+      float pf[64];
       {
         uint32_t sv[64];
-        tmem_ld32(tmem + lane_off + 64 * w, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_ld32(tmem + lane_off + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_ld32(tS + lane_off + 64 * w, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(tS + lane_off + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          float pv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int qq = c + u;
-            float pr = ex2(fmaf(__uint_as_float(sv[qq]), p.scale_log2, -wl[qq]));
-            if (!kv_ok || (diag && 64 * w + qq < r)) pr = 0.0f;
-            pv[u] = pr;
-          }
-          pk[c / 2] = pack_bf16(pv[0], pv[1]);
+        for (int qq = 0; qq < 64; ++qq) {
+          float pr = ex2(fmaf(__uint_as_float(sv[qq]), p.scale_log2, -wl[qq]));
+          if (!kv_ok || (diag && 64 * w + qq < r)) pr = 0.0f;
+          pf[qq] = pr;
         }
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(pf[2 * c], pf[2 * c + 1]);
+        tmem_st32(tS + lane_off + 64 * w, pk);
       }
-      tmem_st32(tmem + lane_off + 64 * w, pk);
       if (!mbar_wait(dp_full, t & 1, p.wc, abort_flag, SITE_BWD_COMPUTE)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      if (t >= 1 && !mbar_wait(ds_free, (t - 1) & 1, p.wc, abort_flag, SITE_BWD_COMPUTE)) {
-        ok = false;
-        break;
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t dp[32];
-        tmem_ld32(tmem + lane_off + 128 + 64 * w + 32 * h, dp);
+      // dS^T = P^T o (dP^T - D) for the same queries, over the dP^T columns
+      {
+        uint32_t dp[64];
+        tmem_ld32(tdP + lane_off + 64 * w, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+        tmem_ld32(tdP + lane_off + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
         tmem_wait_ld();
-        uint32_t dd[16];
+        uint32_t dk[32];
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const int qq = 32 * h + k;
-          const uint32_t pp = pk[qq / 2];
-          const float p0 = __uint_as_float(pp << 16), p1 = __uint_as_float(pp & 0xffff0000u);
-          dd[k / 2] = pack_bf16(p0 * (__uint_as_float(dp[k]) - wd[qq]),
-                                p1 * (__uint_as_float(dp[k + 1]) - wd[qq + 1]));
-        }
-        // queries [64w + 32h, +32) = chunks 4h..4h+3 of half w of the dS^T tile
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          st_shared_v4(sdST + w * (BM * 128) + sw128_off(r, 4 * h + u), dd[4 * u], dd[4 * u + 1],
-                       dd[4 * u + 2], dd[4 * u + 3]);
+        for (int c = 0; c < 32; ++c)
+          dk[c] = pack_bf16(pf[2 * c] * (__uint_as_float(dp[2 * c]) - wd[2 * c]),
+                            pf[2 * c + 1] * (__uint_as_float(dp[2 * c + 1]) - wd[2 * c + 1]));
+        tmem_st32(tdP + lane_off + 64 * w, dk);
       }
-      fence_proxy_async_smem();
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_ready);
@@ -434,33 +387,248 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // --------------------------------------------------- dK, dV epilogue
     if (ok && T > 0 && mbar_wait(fin, 0, p.wc, abort_flag, SITE_BWD_EPI)) {
       tc_fence_after();
-      // WG0 writes dV, WG1 writes dK (times scale)
-      const uint32_t col = 256 + w * D;
-      const float mul = w ? p.scale : 1.0f;
+      // warpgroup 0 writes dV, warpgroup 1 writes dK (times scale)
       __nv_bfloat16 *row = (w ? p.dK : p.dV) + ((int64_t)bh * p.n + kv_idx) * D;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t a[32];
-        tmem_ld32(tmem + lane_off + col + c * 32, a);
-        tmem_wait_ld();
-        if (kv_ok) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(a[8 * k + 0]) * mul, __uint_as_float(a[8 * k + 1]) * mul);
-            v.y = pack_bf16(__uint_as_float(a[8 * k + 2]) * mul, __uint_as_float(a[8 * k + 3]) * mul);
-            v.z = pack_bf16(__uint_as_float(a[8 * k + 4]) * mul, __uint_as_float(a[8 * k + 5]) * mul);
-            v.w = pack_bf16(__uint_as_float(a[8 * k + 6]) * mul, __uint_as_float(a[8 * k + 7]) * mul);
-            reinterpret_cast<uint4 *>(row + c * 32)[k] = v;
-          }
-        }
-      }
+      store_row_bf16<D>((w ? tdK : tdV) + lane_off, row, w ? p.scale : 1.0f, kv_ok);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 13) {
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------ dQ kernel
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
+                  const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmdO, const BwdParams p) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::B_BAR);
+  uint64_t *qd_full = bars + 0;
+  uint64_t *k_full = bars + 1;   // [2]
+  uint64_t *k_empty = bars + 3;  // [2]
+  uint64_t *v_full = bars + 5;   // [2]
+  uint64_t *v_empty = bars + 7;  // [2]
+  uint64_t *s_full = bars + 9;   // [2]
+  uint64_t *dp_full = bars + 11;
+  uint64_t *p_ready = bars + 12;  // 256 arrivals
+  uint64_t *fin = bars + 13;
+  uint64_t *mma_drain = bars + 14;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::B_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::B_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // head-major, heaviest (last) causal query tile first within a head
+  const int bh = blockIdx.x / p.nb;
+  const int ib = p.causal ? (p.nb - 1 - (int)(blockIdx.x % p.nb)) : (int)(blockIdx.x % p.nb);
+  const int NJ = p.causal ? ib + 1 : p.nb;
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 15; ++b) mbar_init(&bars[b], &bars[b] == p_ready ? 256u : 1u);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // S buffers [0,128) and [128,256), dP [256,384), dQ [384, 384+D)
+  const uint32_t tdP = tmem + 256, tdQ = tmem + 384;
+
+  if (warp == 8) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int k_issued = 0, v_issued = 0;
+      mbar_arrive_expect_tx(qd_full, 2 * L::T_BYTES);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(smem + L::B_Q + c * (BM * 128), &tmQ, qd_full, c * 64, ib * BM, bh);
+        tma_load_3d(smem + L::B_DO + c * (BM * 128), &tmdO, qd_full, c * 64, ib * BM, bh);
+      }
+      for (int j = 0; j < NJ; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(&k_empty[s], ((j >> 1) - 1) & 1, p.wc, abort_flag, SITE_DQ_PROD))
+          break;
+        mbar_arrive_expect_tx(&k_full[s], L::T_BYTES);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + L::B_K + s * L::T_BYTES + c * (BM * 128), &tmK, &k_full[s], c * 64,
+                      j * BM, bh);
+        k_issued = j + 1;
+        if (j >= 2 && !mbar_wait(&v_empty[s], ((j >> 1) - 1) & 1, p.wc, abort_flag, SITE_DQ_PROD))
+          break;
+        mbar_arrive_expect_tx(&v_full[s], L::T_BYTES);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + L::B_V + s * L::T_BYTES + c * (BM * 128), &tmV, &v_full[s], c * 64,
+                      j * BM, bh);
+        v_issued = j + 1;
+      }
+      if (*abort_flag) {
+        drain_wait(qd_full, 0, p.wc);
+        for (int j = (k_issued > 2 ? k_issued - 2 : 0); j < k_issued; ++j)
+          drain_wait(&k_full[j & 1], (j >> 1) & 1, p.wc);
+        for (int j = (v_issued > 2 ? v_issued - 2 : 0); j < v_issued; ++j)
+          drain_wait(&v_full[j & 1], (j >> 1) & 1, p.wc);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0);  // S, dP
+      const uint32_t id_q = idesc_bf16_f32(BM, D, 0, 1);   // dQ (A in tensor memory)
+      const uint32_t sQ = smem_u32(smem + L::B_Q);
+      const uint32_t sdO = smem_u32(smem + L::B_DO);
+      const uint32_t sK0 = smem_u32(smem + L::B_K);
+      const uint32_t sV0 = smem_u32(smem + L::B_V);
+      auto issue_s = [&](int j) -> bool {  // S(j) = Q K_j^T into buffer j&1
+        if (!mbar_wait(&k_full[j & 1], (j >> 1) & 1, p.wc, abort_flag, SITE_DQ_MMA)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          umma_f16_ss(tmem + (j & 1) * 128, sdesc_sw128(sQ + off, 16, 1024),
+                      sdesc_sw128(sK0 + (j & 1) * L::T_BYTES + off, 16, 1024), id_s,
+                      kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[j & 1]);
+        return true;
+      };
+      auto issue_dp = [&](int j) -> bool {  // dP(j) = dO V_j^T
+        if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, p.wc, abort_flag, SITE_DQ_MMA)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          umma_f16_ss(tdP, sdesc_sw128(sdO + off, 16, 1024),
+                      sdesc_sw128(sV0 + (j & 1) * L::T_BYTES + off, 16, 1024), id_s,
+                      kk > 0 ? 1u : 0u);
+        }
+        umma_commit(dp_full);
+        umma_commit(&v_empty[j & 1]);  // V_j is read by dP(j) only
+        return true;
+      };
+      bool ok = mbar_wait(qd_full, 0, p.wc, abort_flag, SITE_DQ_MMA) && issue_s(0) && issue_dp(0);
+      for (int j = 0; ok && j < NJ; ++j) {
+        // S(j+1) into the other buffer while the warpgroups work on tile j;
+        // that buffer's dS(j-1) was consumed by dQ(j-1), issued earlier
+        if (j + 1 < NJ && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(p_ready, j & 1, p.wc, abort_flag, SITE_DQ_MMA)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // dQ += dS(j) K_j: keys [64w, 64w+64) of dS sit packed in columns
+        // [64w, 64w+32) of S buffer j&1
+        const uint32_t tA = tmem + (j & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          umma_f16_ts(tdQ, tA + (kk >> 2) * 64 + (kk & 3) * 8,
+                      sdesc_sw128(sK0 + (j & 1) * L::T_BYTES + kk * 2048, BM * 128, 1024), id_q,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&k_empty[j & 1]);
+        if (j + 1 < NJ && !issue_dp(j + 1)) {
+          ok = false;
+          break;
+        }
+      }
+      if (ok) umma_commit(fin);
+      umma_commit(mma_drain);
+      drain_wait(mma_drain, 0, p.wc);
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------- compute (two warpgroups)
+    // Warpgroup w takes keys [64w, 64w+64) of each tile; thread r owns query
+    // row ib*128 + r (tensor-memory lane r), whose LSE and D are constants.
+    const int w = warp >> 2;
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int q_idx = ib * BM + r;
+    const bool q_ok = q_idx < p.n;
+    const float lse2 = q_ok ? p.LSE[(int64_t)bh * p.n + q_idx] * 1.4426950408889634f : INFINITY;
+    const float dval = q_ok ? p.Dvec[(int64_t)bh * p.n + q_idx] : 0.0f;
+    bool ok = true;
+    for (int j = 0; j < NJ; ++j) {
+      const bool masked = (p.causal && j == ib) || ((j + 1) * BM > p.n);
+      const uint32_t tSb = tmem + (j & 1) * 128 + lane_off + 64 * w;
+      if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, p.wc, abort_flag, SITE_DQ_COMPUTE)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float pf[64];
+      {
+        uint32_t sv[64];
+        tmem_ld32(tSb, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(tSb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          float pr = ex2(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lse2));
+          if (masked) {
+            const int kv = j * BM + 64 * w + c;
+            if ((p.causal && kv > q_idx) || kv >= p.n) pr = 0.0f;
+          }
+          pf[c] = pr;
+        }
+      }
+      if (!mbar_wait(dp_full, j & 1, p.wc, abort_flag, SITE_DQ_COMPUTE)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        uint32_t dp[64];
+        tmem_ld32(tdP + lane_off + 64 * w, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+        tmem_ld32(tdP + lane_off + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+        tmem_wait_ld();
+        uint32_t ds[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          ds[c] = pack_bf16(pf[2 * c] * (__uint_as_float(dp[2 * c]) - dval),
+                            pf[2 * c + 1] * (__uint_as_float(dp[2 * c + 1]) - dval));
+        tmem_st32(tSb, ds);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+    }
+    // -------------------------------------------------------- dQ epilogue
+    if (ok && mbar_wait(fin, 0, p.wc, abort_flag, SITE_DQ_EPI)) {
+      tc_fence_after();
+      // warpgroup w writes columns [w D/2, (w+1) D/2) of dQ row q_idx
+      __nv_bfloat16 *row = p.dQ + ((int64_t)bh * p.n + q_idx) * D + w * (D / 2);
+      store_row_bf16<D / 2>(tdQ + lane_off + w * (D / 2), row, p.scale, q_ok);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -476,7 +644,7 @@ cudaError_t launch_bwd_d(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t s
     const unsigned grid = (unsigned)((threads + 255) / 256);
     bwd_prep_kernel<D><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(a.O),
                                              static_cast<const __nv_bfloat16 *>(a.dO), a.Dvec,
-                                             a.dq_acc, rows);
+                                             rows);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   CUtensorMap mq, mk, mv, mdo;
@@ -490,32 +658,29 @@ cudaError_t launch_bwd_d(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t s
   BwdParams p;
   p.BH = a.BH;
   p.n = a.n;
-  p.nqb = (a.n + BM - 1) / BM;
+  p.nb = (a.n + BM - 1) / BM;
   p.causal = a.causal;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.LSE = a.LSE;
   p.Dvec = a.Dvec;
-  p.dq_acc = a.dq_acc;
+  p.dQ = static_cast<__nv_bfloat16 *>(a.dQ);
   p.dK = static_cast<__nv_bfloat16 *>(a.dK);
   p.dV = static_cast<__nv_bfloat16 *>(a.dV);
   p.wc = wc;
-  auto kern = attn_bwd_kernel<D>;
-  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC)))
+  auto ka = bwd_dkdv_kernel<D>;
+  auto kb = bwd_dq_kernel<D>;
+  if ((e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, L::A_ALLOC)))
     return e;
+  if ((e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, L::B_ALLOC)))
+    return e;
+  const unsigned grid = (unsigned)(p.nb * a.BH);
   timing_mark_start(st);
-  kern<<<(unsigned)(p.nqb * a.BH), NTHREADS, L::ALLOC, st>>>(mq, mk, mv, mdo, p);
-  timing_mark_stop(st);
+  ka<<<grid, NTHREADS, L::A_ALLOC, st>>>(mq, mk, mv, mdo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  {
-    const int64_t n8 = rows * D / 8;
-    int64_t grid = (n8 + 255) / 256;
-    if (grid > 152 * 16) grid = 152 * 16;
-    bwd_dq_cvt_kernel<<<(unsigned)grid, 256, 0, st>>>(a.dq_acc, static_cast<__nv_bfloat16 *>(a.dQ),
-                                                      n8);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  kb<<<grid, NTHREADS, L::B_ALLOC, st>>>(mq, mk, mv, mdo, p);
+  timing_mark_stop(st);
+  return cudaGetLastError();
 }
 
 }  // namespace

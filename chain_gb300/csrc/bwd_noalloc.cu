@@ -1,8 +1,8 @@
 // bwd_noalloc.cu -- the attention backward for callers that cannot
 // allocate device memory (chain_bwd_noalloc in include/chain.h).
 //
-// chain_bwd runs three kernels that keep an fp32 accumulator for dQ and an
-// fp32 row term D in a scratch workspace the caller passes in.  Here that
+// chain_bwd keeps an fp32 row term D (one value per query row) in a
+// scratch workspace the caller passes in.  Here that
 // scratch is a fixed array compiled into the library instead, so a caller
 // with no allocator at hand (a pre-reserved memory pool it cannot reach, a
 // plugin that must not grow the device footprint, a loop that cannot take
@@ -55,9 +55,9 @@ extern "C" int chain_bwd_noalloc(const chain_tensor_t *dO, const chain_tensor_t 
     }
     scratch = g_noalloc_addr[dev];
   }
-  // Same checks and kernels as chain_bwd; the preprocess kernel re-zeroes
-  // the dQ accumulator and rewrites D on every call, so what an earlier call
-  // left in the array is never read.
+  // Same checks and kernels as chain_bwd; the preprocess kernel rewrites D
+  // for every row on every call, so what an earlier call left in the array
+  // is never read.
   return chain_bwd(dO, A, B, C, O, LSE, f, mask, scale, dA, dB, dC, scratch,
                    CHAIN_NOALLOC_SCRATCH_BYTES, stream);
 }

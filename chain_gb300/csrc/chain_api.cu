@@ -335,9 +335,8 @@ size_t chain_bwd_workspace_size(const chain_tensor_t *A, const chain_tensor_t *C
   View a, c;
   if (view_of(A, 2, &a) || view_of(C, 2, &c)) return 0;
   if (!same_shape(a, c)) return 0;
-  const size_t acc = (size_t)a.outer * a.rows * a.cols * sizeof(float);
   const size_t dvec = (size_t)a.outer * a.rows * sizeof(float);
-  return ((acc + 255) & ~size_t(255)) + ((dvec + 255) & ~size_t(255));
+  return (dvec + 255) & ~size_t(255);
 }
 
 int chain_bwd(const chain_tensor_t *dO, const chain_tensor_t *A, const chain_tensor_t *B,
@@ -376,10 +375,7 @@ int chain_bwd(const chain_tensor_t *dO, const chain_tensor_t *A, const chain_ten
   args.Q = q.ptr; args.K = k.ptr; args.V = v.ptr; args.O = o.ptr; args.dO = g.ptr;
   args.LSE = static_cast<const float *>(LSE->ptr);
   args.dQ = dq.ptr; args.dK = dk.ptr; args.dV = dv.ptr;
-  const size_t acc = (size_t)q.outer * q.rows * q.cols * sizeof(float);
-  args.dq_acc = static_cast<float *>(workspace);
-  args.Dvec = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                        ((acc + 255) & ~size_t(255)));
+  args.Dvec = static_cast<float *>(workspace);
   args.BH = (int)q.outer; args.n = (int)q.rows; args.d = (int)q.cols;
   args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
   DevInfo *di = nullptr;

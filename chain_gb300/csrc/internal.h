@@ -33,7 +33,6 @@ struct AttnBwdArgs {
   const void *Q, *K, *V, *O, *dO;  // bf16 [BH][n][d], row stride d, head stride n*d
   const float *LSE;                // [BH][n]
   void *dQ, *dK, *dV;              // bf16 [BH][n][d]
-  float *dq_acc;                   // fp32 [BH][n][d] workspace
   float *Dvec;                     // fp32 [BH][n] workspace
   int BH, n, d, causal;
   float scale;

@@ -107,8 +107,8 @@ int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B,
 
 /*
  * chain_bwd_workspace_size -- bytes of device workspace chain_bwd needs for
- * these shapes (an fp32 [BH][n][d] accumulator for dA plus an fp32 [BH][n]
- * row term).  Returns 0 for invalid descriptors.
+ * these shapes: the fp32 [BH][n] row term D, rounded up to 256 bytes.
+ * Returns 0 for invalid descriptors.
  */
 size_t chain_bwd_workspace_size(const chain_tensor_t *A, const chain_tensor_t *C);
 
@@ -119,7 +119,9 @@ size_t chain_bwd_workspace_size(const chain_tensor_t *A, const chain_tensor_t *C
  *   f = CHAIN_F_SOFTMAX with bf16 and d in {64, 128} is supported.
  *   Outputs: dQ (dA), dK (dB), dV (dC) [BH][n][d] bf16.
  *   S and P are recomputed per tile from LSE ("recompute, don't store",
- *   AutoSP 2.B); D_i = sum_e dO_ie O_ie.
+ *   AutoSP 2.B); D_i = sum_e dO_ie O_ie.  dK, dV come from one pass over
+ *   the key blocks and dQ from a second over the query tiles, each
+ *   accumulating on chip: no atomics, results are deterministic.
  *   workspace: device buffer of at least chain_bwd_workspace_size() bytes,
  *   16-byte aligned, contents ignored on entry.
  */
@@ -147,8 +149,8 @@ int chain_bwd(const chain_tensor_t *dO, const chain_tensor_t *A,
  * exits.  It never calls cudaMalloc, cudaFree or any allocating routine.
  *
  * Limit: chain_bwd_workspace_size(A, C) must not exceed
- * CHAIN_NOALLOC_SCRATCH_BYTES (for d = 128: BH * n <= 65,027 rows), else
- * the call returns CHAIN_ERR_SCRATCH_LIMIT before enqueuing anything.
+ * CHAIN_NOALLOC_SCRATCH_BYTES (BH * n <= 8,388,608 rows), else the call
+ * returns CHAIN_ERR_SCRATCH_LIMIT before enqueuing anything.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture begins.

@@ -39,11 +39,29 @@ def test_noalloc_matches_chain_bwd_on_two_calls(cg):
 
 
 def test_noalloc_rejects_problem_beyond_scratch(cg):
-    BH, n, d = 16, 8192, 128  # needs 16*8192*(128+1)*4 bytes > 32 MiB
-    q = torch.zeros(BH, n, d, dtype=torch.bfloat16, device="cuda")
-    lse = torch.zeros(BH, n, dtype=torch.float32, device="cuda")
-    assert cg.chain_bwd_workspace_size(q, q) > cg.NOALLOC_SCRATCH_BYTES
-    out = [torch.empty_like(q) for _ in range(3)]
-    with pytest.raises(cg.ChainError) as ei:
-        cg.chain_bwd_noalloc(q, q, q, q, q, lse, cg.F_SOFTMAX, cg.MASK_CAUSAL, 0.1, *out)
-    assert ei.value.status == cg.ERR_SCRATCH_LIMIT
+    # A problem whose row term needs more than the fixed scratch: 9 * 2^20
+    # rows of d = 128 (the descriptors are checked before any memory is
+    # touched, so they may describe more rows than the buffers hold).
+    import ctypes
+    q = torch.zeros(1, 128, 128, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(1, 128, dtype=torch.float32, device="cuda")
+    BH, n = 9, 1 << 20
+
+    def big(t, lse_like=False):
+        d = cg.desc(t)
+        if lse_like:
+            d.ndim, d.shape[0], d.shape[1], d.stride[0], d.stride[1] = 2, BH, n, n, 1
+        else:
+            d.ndim = 3
+            d.shape[0], d.shape[1], d.shape[2] = BH, n, 128
+            d.stride[0], d.stride[1], d.stride[2] = n * 128, 128, 1
+        return d
+
+    ds = [big(q) for _ in range(8)]
+    dl = big(lse, lse_like=True)
+    assert cg.lib().chain_bwd_workspace_size(ctypes.byref(ds[1]), ctypes.byref(ds[3])) > \
+        cg.NOALLOC_SCRATCH_BYTES
+    rc = cg.lib().chain_bwd_noalloc(*(ctypes.byref(d) for d in ds[:5]), ctypes.byref(dl),
+                                    cg.F_SOFTMAX, cg.MASK_CAUSAL, ctypes.c_float(0.1),
+                                    *(ctypes.byref(d) for d in ds[5:]), None)
+    assert rc == cg.ERR_SCRATCH_LIMIT
