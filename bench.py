@@ -242,7 +242,7 @@ class HotPath:
                               flops=mlp_flops(m["M"], m["K"], m["N"], m["P"]), bytes=0.0, launches=1,
                               fn=lambda: cg.chain_fwd(self.x, self.w1, self.w2, cg.F_GELU_TANH, 0, 1.0,
                                                       self.o2, None)))
-        comps.append(dict(name="attn_bwd_causal_16x65536x128", kernel="attn_bwd_kernel",
+        comps.append(dict(name="attn_bwd_causal_16x65536x128", kernel="bwd_dkdv_kernel+bwd_dq_kernel",
                           flops=attn_bwd_flops(b["BH"], b["n"], b["d"], True), bytes=0.0, launches=3,
                           fn=lambda: cg.chain_bwd(self.do5, self.q5, self.k5, self.v5, self.o5, self.l5,
                                                   cg.F_SOFTMAX, cg.MASK_CAUSAL, b["d"] ** -0.5,
@@ -304,16 +304,18 @@ def barrier(dist):
 
 
 def max_over_ranks(x, dist):
+    """Max of a host scalar over all ranks (the timing rule of multi-GPU runs)."""
     if dist is None:
         return x
     import torch
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
 
 # ------------------------------------------------------- CPU baseline
-def oracle_sample(scale: int = 1):
+def oracle_sample(scale: int = 2):
     """Time the fp64 oracle on a bounded sample of the same workloads (about
     15 s of host work at scale 1); returns (TFLOP/s, seconds, description,
     threads)."""
@@ -326,7 +328,7 @@ def oracle_sample(scale: int = 1):
     # attention forward rows of the 32k workload (one head), causal
     c3 = W["causal_attn_32k"].dims
     q, k, v = cs.attn_inputs(2, c3["n"], c3["d"], seed=W["causal_attn_32k"].seed)
-    nr = 6144 * scale
+    nr = 4096 * scale
     rows = [(h, r) for h in range(2) for r in range(c3["n"] - nr // 2, c3["n"])]
     t0 = time.perf_counter()
     oracle.softmax_fwd(q, k, v, c3["d"] ** -0.5, True, rows=rows)
@@ -337,7 +339,7 @@ def oracle_sample(scale: int = 1):
     # backward: last 16 query rows of the 64k workload, one head
     b = W["causal_bwd_64k"].dims
     q, k, v, do = cs.attn_inputs(1, b["n"], b["d"], seed=W["causal_bwd_64k"].seed, with_do=True)
-    i0 = b["n"] - 1536 * scale
+    i0 = b["n"] - 1024 * scale
     t0 = time.perf_counter()
     oracle.softmax_bwd(q, k, v, do, b["d"] ** -0.5, True, row_range=(i0, b["n"]),
                        col_range=(i0, b["n"]))
@@ -348,7 +350,7 @@ def oracle_sample(scale: int = 1):
     # MLP rows
     m = W["gelu_mlp"].dims
     x, w1, w2 = cs.mlp_inputs(m["M"], m["K"], m["N"], m["P"], seed=W["gelu_mlp"].seed)
-    rows = list(range(0, m["M"]))
+    rows = [r % m["M"] for r in range(0, m["M"] * scale // 2)]
     t0 = time.perf_counter()
     oracle.chain_fwd(x, w1, w2, oracle.F_GELU_TANH, rows=rows)
     dt = time.perf_counter() - t0
