@@ -42,6 +42,23 @@ WORKLOAD = ("chain hot path: 3x sp_relayout 4x[32768][32][128]->[8][131072][128]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def measured_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/traffic.json), or None once the kernel's source file has
+    changed since the counters were taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            entry = json.load(f).get(kernel)
+        if not entry:
+            return None
+        with open(os.path.join(ROOT, entry["source"]), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        return entry["dram_bytes_per_launch"] if sha == entry["source_sha256_16"] else None
+    except (OSError, ValueError, KeyError):
+        return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -226,42 +243,55 @@ class HotPath:
         Hl, N = u["H"] // u["p"], u["p"] * u["n_loc"]
         comps = []
         for t in range(3):
-            comps.append(dict(name=f"sp_relayout[{'QKV'[t]}]", kernel="relayout_kernel", flops=0.0,
+            comps.append(dict(name=f"sp_relayout[{'QKV'[t]}]", flops=0.0,
                               bytes=2.0 * Hl * N * u["d"] * 2, launches=1,
+                              kernels=[("relayout_kernel", 0.0, 2.0 * Hl * N * u["d"] * 2)],
                               fn=(lambda t=t: cg.sp_relayout(self.shards[t], u["p"], u["g"], self.hm[t]))))
-        comps.append(dict(name="attn_fwd_causal_8x131072x128", kernel="attn_fwd_kernel", flops=attn_fwd_flops(Hl, N, u["d"], True),
+        comps.append(dict(name="attn_fwd_causal_8x131072x128", flops=attn_fwd_flops(Hl, N, u["d"], True),
                           bytes=0.0, launches=1,
+                          kernels=[("attn_fwd_kernel", attn_fwd_flops(Hl, N, u["d"], True), 0.0)],
                           fn=lambda: cg.chain_fwd(self.hm[0], self.hm[1], self.hm[2], cg.F_SOFTMAX,
                                                   cg.MASK_CAUSAL, u["d"] ** -0.5, self.o4, self.l4)))
-        comps.append(dict(name="attn_fwd_causal_32x32768x128", kernel="attn_fwd_kernel",
+        comps.append(dict(name="attn_fwd_causal_32x32768x128",
                           flops=attn_fwd_flops(c3["BH"], c3["n"], c3["d"], True), bytes=0.0, launches=1,
+                          kernels=[("attn_fwd_kernel", attn_fwd_flops(c3["BH"], c3["n"], c3["d"], True),
+                                    0.0)],
                           fn=lambda: cg.chain_fwd(self.q3, self.k3, self.v3, cg.F_SOFTMAX,
                                                   cg.MASK_CAUSAL, c3["d"] ** -0.5, self.o3, self.l3)))
         if self.mlp_ok:
-            comps.append(dict(name="gelu_mlp_4096x1024x4096x1024", kernel="mlp_chain_kernel",
+            comps.append(dict(name="gelu_mlp_4096x1024x4096x1024",
                               flops=mlp_flops(m["M"], m["K"], m["N"], m["P"]), bytes=0.0, launches=1,
+                              kernels=[("mlp_chain_kernel", mlp_flops(m["M"], m["K"], m["N"], m["P"]),
+                                        0.0)],
                               fn=lambda: cg.chain_fwd(self.x, self.w1, self.w2, cg.F_GELU_TANH, 0, 1.0,
                                                       self.o2, None)))
-        comps.append(dict(name="attn_bwd_causal_16x65536x128", kernel="bwd_dkdv_kernel+bwd_dq_kernel",
-                          flops=attn_bwd_flops(b["BH"], b["n"], b["d"], True), bytes=0.0, launches=3,
+        fb = attn_bwd_flops(b["BH"], b["n"], b["d"], True)
+        # of the 5 counted products, dK/dV makes S, dP, dV, dK and dQ makes dQ
+        # (its recomputed S and dP are not counted)
+        comps.append(dict(name="attn_bwd_causal_16x65536x128", flops=fb, bytes=0.0, launches=3,
+                          kernels=[("bwd_dkdv_kernel", 0.8 * fb, 0.0), ("bwd_dq_kernel", 0.2 * fb, 0.0)],
                           fn=lambda: cg.chain_bwd(self.do5, self.q5, self.k5, self.v5, self.o5, self.l5,
                                                   cg.F_SOFTMAX, cg.MASK_CAUSAL, b["d"] ** -0.5,
                                                   self.dq5, self.dk5, self.dv5, self.ws)))
         if self.fp32_ok:
-            comps.append(dict(name="attn_fwd_fp32_1x256x64", kernel="attn_fwd_f32_kernel",
+            comps.append(dict(name="attn_fwd_fp32_1x256x64",
                               flops=attn_fwd_flops(1, t1["n"], t1["d"], False), bytes=0.0, launches=1,
+                              kernels=[("attn_fwd_f32_kernel", attn_fwd_flops(1, t1["n"], t1["d"], False),
+                                        0.0)],
                               fn=lambda: cg.chain_fwd(self.q1, self.k1, self.v1, cg.F_SOFTMAX,
                                                       cg.MASK_NONE, t1["d"] ** -0.5, self.o1,
                                                       self.l1)))
         return comps
 
     def step(self, events=None):
+        """One pass over every component; events[i] (len(kernels) + 1 CUDA
+        events) are recorded at the main-kernel boundaries of component i."""
         for i, c in enumerate(self.comp):
             if events is not None:
                 self.cg.set_timing_events(*events[i])
             c["fn"]()
         if events is not None:
-            self.cg.set_timing_events(None, None)
+            self.cg.set_timing_events()
 
     # host <-> device for the end-to-end number
     def host_io(self):
@@ -422,8 +452,8 @@ def main():
         raise RuntimeError(f"device status {rc} site {site:#x} after warm-up")
 
     # ---- timed region (kernels only, inputs resident)
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(ncomp)] for _ in range(args.steps)]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(c["kernels"]) + 1)]
+             for c in hp.comp] for _ in range(args.steps)]
     clk = ClockSampler(local)
     clk.start()
     time.sleep(0.3)
@@ -445,8 +475,21 @@ def main():
     if rc != 0:
         raise RuntimeError(f"device status {rc} site {site:#x} in timed region")
 
-    comp_ms = [statistics.mean(evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps))
-               for i in range(ncomp)]
+    # per component: device time of its main kernels; per kernel function:
+    # summed time, algorithmic work and launches over the step
+    comp_ms, by_k = [], {}
+    for i, c in enumerate(hp.comp):
+        tot = 0.0
+        for k, (kname, kflops, kbytes) in enumerate(c["kernels"]):
+            ms = statistics.mean(evs[s][i][k].elapsed_time(evs[s][i][k + 1])
+                                 for s in range(args.steps))
+            tot += ms
+            e = by_k.setdefault(kname, {"ms": 0.0, "flops": 0.0, "bytes": 0.0, "launches": 0})
+            e["ms"] += ms
+            e["flops"] += kflops
+            e["bytes"] += kbytes
+            e["launches"] += 1
+        comp_ms.append(tot)
     tf_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     components = {}
@@ -462,32 +505,29 @@ def main():
         components[c["name"]] = e
     # dominant kernel: the kernel function with the largest share of the
     # step's device time; achieved = its algorithmic work / its time, summed
-    # over its launches in the step (one launch per component).
-    by_k = {}
-    for c, ms in zip(hp.comp, comp_ms):
-        k = by_k.setdefault(c["kernel"], {"ms": 0.0, "flops": 0.0, "bytes": 0.0, "launches": 0})
-        k["ms"] += ms
-        k["flops"] += c["flops"]
-        k["bytes"] += c["bytes"]
-        k["launches"] += 1
+    # over its launches in the step.
     dom_name = max(by_k, key=lambda k: by_k[k]["ms"])
     dom = by_k[dom_name]
     share = dom["ms"] / sum(v["ms"] for v in by_k.values())
     if dom["flops"]:
         ach = dom["flops"] / (dom["ms"] * 1e-3) / 1e12
         roof = {"kernel": dom_name, "bound": "tensor", "achieved": round(ach, 1),
+                "kernel_shares": {k: round(v["ms"] / sum(x["ms"] for x in by_k.values()), 4)
+                                  for k, v in by_k.items()},
                 "peak": tf_peak, "unit": "TFLOP/s", "frac": round(ach / tf_peak, 4),
                 "peak_source": f"{peak_src} bf16_tflops_sustained",
                 "launches_per_step": dom["launches"], "flops_per_step": dom["flops"],
                 "avg_launch_ms": round(dom["ms"] / dom["launches"], 4),
-                "share_of_step_device_time": round(share, 4), "traffic": None}
+                "share_of_step_device_time": round(share, 4),
+                "traffic": measured_traffic(dom_name), "traffic_unit": "bytes per launch (ncu)"}
     else:
         ach = dom["bytes"] / (dom["ms"] * 1e-3) / 1e9
         roof = {"kernel": dom_name, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
                 "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "peak_source": f"{peak_src} hbm_gbs",
                 "launches_per_step": dom["launches"], "bytes_per_step": dom["bytes"],
                 "avg_launch_ms": round(dom["ms"] / dom["launches"], 4),
-                "share_of_step_device_time": round(share, 4), "traffic": None}
+                "share_of_step_device_time": round(share, 4),
+                "traffic": measured_traffic(dom_name), "traffic_unit": "bytes per launch (ncu)"}
     flops_all = hp.flops * world
     value = flops_all / (ms_step * 1e-3) / 1e12
 

@@ -75,7 +75,7 @@ def _load():
             lib.chain_check.argtypes = [vp, ctypes.POINTER(ci)]
             lib.chain_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
             lib.chain_set_wait_limit_ns.restype = None
-            lib.chain_set_timing_events.argtypes = [vp, vp]
+            lib.chain_set_timing_events.argtypes = [ctypes.POINTER(vp), ci]
             lib.chain_set_timing_events.restype = None
             lib.chain_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
             lib.chain_umma_selftest.argtypes = [vp, vp, vp, ci, ci, ci, vp]
@@ -188,15 +188,15 @@ def set_wait_limit_ns(ns: int):
     _load().chain_set_wait_limit_ns(int(ns))
 
 
-def set_timing_events(start=None, stop=None):
-    """Record torch.cuda.Event ``start``/``stop`` around the main kernel of
-    subsequent calls from this thread (None, None clears)."""
-    for ev in (start, stop):
-        if ev is not None and ev.cuda_event == 0:
+def set_timing_events(*events):
+    """Record torch.cuda.Event objects at the main-kernel boundaries of
+    subsequent calls from this thread (events[0] before the first main
+    kernel, events[k] after the k-th); no arguments clears."""
+    for ev in events:
+        if ev.cuda_event == 0:
             ev.record()  # torch creates the underlying event on first record
-    _load().chain_set_timing_events(
-        ctypes.c_void_p(start.cuda_event if start is not None else 0),
-        ctypes.c_void_p(stop.cuda_event if stop is not None else 0))
+    arr = (ctypes.c_void_p * max(1, len(events)))(*[ev.cuda_event for ev in events])
+    _load().chain_set_timing_events(arr if events else None, len(events))
 
 
 def selftest_wait_timeout(limit_ns: int, stream=None):

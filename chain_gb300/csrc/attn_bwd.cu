@@ -675,11 +675,12 @@ cudaError_t launch_bwd_d(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t s
   if ((e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, L::B_ALLOC)))
     return e;
   const unsigned grid = (unsigned)(p.nb * a.BH);
-  timing_mark_start(st);
+  timing_mark(st, 0);
   ka<<<grid, NTHREADS, L::A_ALLOC, st>>>(mq, mk, mv, mdo, p);
+  timing_mark(st, 1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   kb<<<grid, NTHREADS, L::B_ALLOC, st>>>(mq, mk, mv, mdo, p);
-  timing_mark_stop(st);
+  timing_mark(st, 2);
   return cudaGetLastError();
 }
 

@@ -443,9 +443,9 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t s
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(p.nqb2 * a.BH);
-  timing_mark_start(st);
+  timing_mark(st, 0);
   kern<<<grid, NTHREADS, L::ALLOC, st>>>(mq, mk, mv, p);
-  timing_mark_stop(st);
+  timing_mark(st, 1);
   return cudaGetLastError();
 }
 

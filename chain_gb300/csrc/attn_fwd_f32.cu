@@ -262,9 +262,9 @@ cudaError_t launch_attn_fwd_f32(const AttnFwdArgs &a, const WaitCfg &wc, cudaStr
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_f32_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  timing_mark_start(st);
+  timing_mark(st, 0);
   attn_fwd_f32_kernel<<<(unsigned)(p.nqb * a.BH), NT, SMEM_ALLOC, st>>>(p);
-  timing_mark_stop(st);
+  timing_mark(st, 1);
   return cudaGetLastError();
 }
 

@@ -15,7 +15,9 @@ __device__ DevStatus g_status;
 namespace {
 
 thread_local int t_last_cuda_error = 0;
-thread_local cudaEvent_t t_ev_start = nullptr, t_ev_stop = nullptr;
+constexpr int kMaxTimingEvents = 4;
+thread_local cudaEvent_t t_events[kMaxTimingEvents] = {};
+thread_local int t_nevents = 0;
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 
 struct DevInfo {
@@ -167,11 +169,8 @@ int lse_view(const chain_tensor_t *t, int64_t BH, int64_t n, int64_t *s_bh) {
 
 int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
 
-void timing_mark_start(cudaStream_t st) {
-  if (t_ev_start) cudaEventRecord(t_ev_start, st);
-}
-void timing_mark_stop(cudaStream_t st) {
-  if (t_ev_stop) cudaEventRecord(t_ev_stop, st);
+void timing_mark(cudaStream_t st, int k) {
+  if (k < t_nevents && t_events[k]) cudaEventRecord(t_events[k], st);
 }
 
 cudaError_t make_tmap(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void *base,
@@ -216,9 +215,13 @@ int chain_last_cuda_error(void) { return t_last_cuda_error; }
 
 void chain_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
 
-void chain_set_timing_events(void *start, void *stop) {
-  t_ev_start = static_cast<cudaEvent_t>(start);
-  t_ev_stop = static_cast<cudaEvent_t>(stop);
+void chain_set_timing_events(void *const *events, int count) {
+  if (!events || count <= 0) {
+    t_nevents = 0;
+    return;
+  }
+  t_nevents = count < kMaxTimingEvents ? count : kMaxTimingEvents;
+  for (int k = 0; k < t_nevents; ++k) t_events[k] = static_cast<cudaEvent_t>(events[k]);
 }
 
 int chain_check(void *stream, int *detail) {

@@ -54,9 +54,8 @@ cudaError_t launch_relayout(const void *in, void *out, int64_t p, int64_t n_loc,
 int record_cuda_error(cudaError_t e);
 
 // Measurement hook (chain_set_timing_events): record the calling thread's
-// start/stop events, if set, around the main kernel of a call.
-void timing_mark_start(cudaStream_t st);
-void timing_mark_stop(cudaStream_t st);
+// event k, if set, at the k-th main-kernel boundary of a call.
+void timing_mark(cudaStream_t st, int k);
 
 cudaError_t launch_wait_selftest(const WaitCfg &wc, cudaStream_t st);
 cudaError_t launch_umma_selftest(const void *A, const void *B, float *D, int N, int K,

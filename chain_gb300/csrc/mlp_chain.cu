@@ -347,9 +347,9 @@ cudaError_t launch_mlp_chain(const MlpArgs &a, const WaitCfg &wc, cudaStream_t s
                                 MlpLayout::ALLOC)))
     return e;
   const unsigned grid = (unsigned)((a.M / BM) * (a.P / BP));
-  timing_mark_start(st);
+  timing_mark(st, 0);
   mlp_chain_kernel<<<grid, NTHREADS, MlpLayout::ALLOC, st>>>(mx, mw1, mw2, p);
-  timing_mark_stop(st);
+  timing_mark(st, 1);
   return cudaGetLastError();
 }
 

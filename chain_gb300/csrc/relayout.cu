@@ -72,11 +72,11 @@ cudaError_t launch_relayout(const void *in, void *out, int64_t p, int64_t n_loc,
   int64_t want = (total + (int64_t)THREADS * UNROLL - 1) / ((int64_t)THREADS * UNROLL);
   const int64_t cap = (int64_t)(sms > 0 ? sms : 152) * 8;
   const unsigned grid = (unsigned)(want < cap ? want : cap);
-  timing_mark_start(st);
+  timing_mark(st, 0);
   relayout_kernel<<<grid, THREADS, 0, st>>>(
       static_cast<const uint4 *>(in), static_cast<uint4 *>(out), (uint32_t)N, (uint32_t)H,
       (uint32_t)Hl, (uint32_t)vrow, (uint32_t)(g * Hl), (uint32_t)total, inverse);
-  timing_mark_stop(st);
+  timing_mark(st, 1);
   return cudaGetLastError();
 }
 

@@ -202,15 +202,16 @@ int chain_check(void *stream, int *detail);
 void chain_set_wait_limit_ns(uint64_t ns);
 
 /*
- * chain_set_timing_events -- measurement hook.  While set (non-NULL), every
+ * chain_set_timing_events -- measurement hook.  While set (count > 0), every
  * chain_fwd / chain_bwd / sp_relayout call issued from the calling host
- * thread records `start` (a cudaEvent_t) on its stream immediately before
- * launching its main kernel and `stop` immediately after it, so the main
- * kernel alone can be timed without the backward's preprocess and dQ
- * conversion kernels.  Pass NULL, NULL to clear.  Events are owned by the
- * caller.
+ * thread records events[k] (cudaEvent_t, k < count) on its stream at the
+ * k-th boundary of its main kernels: events[0] just before the first main
+ * kernel, events[1] just after it, events[2] after the second (the
+ * backward has two main kernels: dK/dV, then dQ; its small preprocess runs
+ * before events[0]).  Boundaries beyond count are not recorded.  Pass
+ * NULL, 0 to clear.  At most 4 events; events are owned by the caller.
  */
-void chain_set_timing_events(void *start, void *stop);
+void chain_set_timing_events(void *const *events, int count);
 
 /*
  * chain_selftest_wait_timeout -- launches one CTA that waits on a barrier
