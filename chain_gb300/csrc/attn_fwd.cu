@@ -84,6 +84,16 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const
   mbar_wait(bar, parity, wc, &never, SITE_FWD_DRAIN);
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
 // Number of key tiles query tile t (0 = a, 1 = b) of 256-row block qb sees.
 __device__ __forceinline__ int kv_tiles(const FwdParams &p, int qb, int t) {
   if (!p.causal) return p.nkb;
@@ -292,25 +302,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int kv0 = j * BN;
       const bool diag = p.causal && (j == 2 * qb + t);
       const bool masked = diag || (kv0 + BN > p.n);
-      // pass 1: row max over the 128 keys (one round trip to tensor memory;
-      // diagonal and ragged tiles mask keys after the row and beyond n)
-      float mx = -INFINITY;
-      {
-        uint32_t s[BN];
+      // Row of S: one round trip to tensor memory, kept in registers for
+      // both passes.  Diagonal and ragged tiles mask keys after the row and
+      // keys beyond n.
+      uint32_t s[BN];
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c)
-          tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
-        tmem_wait_ld();
-        if (masked) {
+      for (int c = 0; c < BN / 32; ++c)
+        tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+      tmem_wait_ld();
+      if (masked) {
 #pragma unroll
-          for (int k = 0; k < BN; ++k) {
-            const int kv = kv0 + k;
-            if ((diag && kv > q_idx) || kv >= p.n) s[k] = __float_as_uint(-INFINITY);
-          }
+        for (int k = 0; k < BN; ++k) {
+          const int kv = kv0 + k;
+          if ((diag && kv > q_idx) || kv >= p.n) s[k] = __float_as_uint(-INFINITY);
         }
-#pragma unroll
-        for (int k = 0; k < BN; ++k) mx = fmaxf(mx, __uint_as_float(s[k]));
       }
+      // pass 1: row max, eight independent partial maxima (a tree, not a
+      // 128-long dependent chain)
+      float mx8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(s[u]);
+#pragma unroll
+      for (int k = 8; k < BN; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(s[k]));
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       mx *= p.scale_log2;  // scale > 0: the max commutes with the scaling
       float alpha = 1.0f;
       bool rescale = false;
@@ -322,8 +337,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         rescale = true;
       }
       const float mref = (m == -INFINITY) ? 0.0f : m;
+      // pass 2: P = 2^(s*scale*log2e - m), 16 keys at a time, written back
+      // over the columns already read: keys [16g, 16g+16) go to columns
+      // [16g, 16g+8) (P_hi) and [16g+8, 16g+16) (P_lo), two keys per column.
+      float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int g = 0; g < BN / 16; ++g) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(s[g * 16 + k]), p.scale_log2, -mref));
+          const float p1 = ex2(fmaf(__uint_as_float(s[g * 16 + k + 1]), p.scale_log2, -mref));
+          rs4[(k >> 1) & 3] += p0 + p1;
+          const uint32_t h = pack_bf16(p0, p1);
+          pk[k >> 1] = h;
+          pk[8 + (k >> 1)] =
+              pack_bf16(p0 - __uint_as_float(h << 16), p1 - __uint_as_float(h & 0xffff0000u));
+        }
+        tmem_st16(tS + g * 16, pk);
+      }
+      const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
       // O_t holds every P_t(j') V_j' with j' < j here: S_t(j) was issued
-      // after PV_t(j-1), and PV_t(j) waits for p_ready below.
+      // after PV_t(j-1), and PV_t(j) waits for p_ready below.  (Done after
+      // pass 2 so the row of S is no longer live.)
       if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -333,40 +369,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
           tmem_st32(tO + c * 32, o);
-        }
-      }
-      // pass 2: P = 2^(s*scale*log2e - m) for 32 keys at a time, written
-      // back over the columns just read: keys [16k, 16k+16) go to columns
-      // [16k, 16k+8) (P_hi) and [16k+8, 16k+16) (P_lo), two keys per column.
-      float rs = 0.0f;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t s[64];
-        tmem_ld32(tS + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-        tmem_ld32(tS + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-        tmem_wait_ld();
-        if (masked) {
-#pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const int kv = kv0 + hf * 64 + k;
-            if ((diag && kv > q_idx) || kv >= p.n) s[k] = __float_as_uint(-INFINITY);
-          }
-        }
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            const float p0 = ex2(fmaf(__uint_as_float(s[c * 32 + k]), p.scale_log2, -mref));
-            const float p1 = ex2(fmaf(__uint_as_float(s[c * 32 + k + 1]), p.scale_log2, -mref));
-            rs += p0 + p1;
-            const uint32_t h = pack_bf16(p0, p1);
-            const int g = k >> 4, w = (k & 15) >> 1;  // 16-key group, pair within it
-            pk[g * 16 + w] = h;
-            pk[g * 16 + 8 + w] =
-                pack_bf16(p0 - __uint_as_float(h << 16), p1 - __uint_as_float(h & 0xffff0000u));
-          }
-          tmem_st32(tS + hf * 64 + c * 32, pk);
         }
       }
       l = l * alpha + rs;
