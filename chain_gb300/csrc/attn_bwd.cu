@@ -344,18 +344,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         break;
       }
       tc_fence_after();
-      // P^T for queries [64w, 64w+64): bf16 pairs over the columns just read
+      // P^T for queries [64w, 64w+64): fp32 exponentials, bf16 pairs written
+      // back over the S^T columns just read
       float pf[64];
       {
         uint32_t sv[64];
         tmem_ld32(tS + lane_off + 64 * w, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
         tmem_ld32(tS + lane_off + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
         tmem_wait_ld();
+        const float4 *wl4 = reinterpret_cast<const float4 *>(wl);
 #pragma unroll
-        for (int qq = 0; qq < 64; ++qq) {
-          float pr = ex2(fmaf(__uint_as_float(sv[qq]), p.scale_log2, -wl[qq]));
-          if (!kv_ok || (diag && 64 * w + qq < r)) pr = 0.0f;
-          pf[qq] = pr;
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 lv = wl4[c4];
+          const float ls[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int qq = 4 * c4 + u;
+            float pr = ex2(fmaf(__uint_as_float(sv[qq]), p.scale_log2, -ls[u]));
+            if (!kv_ok || (diag && 64 * w + qq < r)) pr = 0.0f;
+            pf[qq] = pr;
+          }
         }
         uint32_t pk[32];
 #pragma unroll
@@ -373,11 +381,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_ld32(tdP + lane_off + 64 * w, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
         tmem_ld32(tdP + lane_off + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
         tmem_wait_ld();
+        const float4 *wd4 = reinterpret_cast<const float4 *>(wd);
         uint32_t dk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          dk[c] = pack_bf16(pf[2 * c] * (__uint_as_float(dp[2 * c]) - wd[2 * c]),
-                            pf[2 * c + 1] * (__uint_as_float(dp[2 * c + 1]) - wd[2 * c + 1]));
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 dv = wd4[c4];
+          const float ds[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int qq = 4 * c4 + 2 * h;
+            dk[qq / 2] = pack_bf16(pf[qq] * (__uint_as_float(dp[qq]) - ds[2 * h]),
+                                   pf[qq + 1] * (__uint_as_float(dp[qq + 1]) - ds[2 * h + 1]));
+          }
+        }
         tmem_st32(tdP + lane_off + 64 * w, dk);
       }
       tmem_wait_st();
