@@ -251,28 +251,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0);  // S^T, dP^T
       const uint32_t id_kv = idesc_bf16_f32(BM, D, 0, 1);  // dV, dK (A in tensor memory)
-      const uint32_t sK = smem_u32(smem + L::A_K);
-      const uint32_t sV = smem_u32(smem + L::A_V);
-      const uint32_t sQ0 = smem_u32(smem + L::A_Q);
-      const uint32_t sdO0 = smem_u32(smem + L::A_DO);
+      // base descriptors, built once (K-major operands, then MN-major views)
+      const SDesc kK = sdesc_make(smem_u32(smem + L::A_K), 16, 1024);
+      const SDesc kV = sdesc_make(smem_u32(smem + L::A_V), 16, 1024);
+      const SDesc kQ0 = sdesc_make(smem_u32(smem + L::A_Q), 16, 1024);
+      const SDesc kQ1 = sdesc_make(smem_u32(smem + L::A_Q + L::T_BYTES), 16, 1024);
+      const SDesc kO0 = sdesc_make(smem_u32(smem + L::A_DO), 16, 1024);
+      const SDesc kO1 = sdesc_make(smem_u32(smem + L::A_DO + L::T_BYTES), 16, 1024);
+      const SDesc mQ0 = sdesc_make(smem_u32(smem + L::A_Q), BM * 128, 1024);
+      const SDesc mQ1 = sdesc_make(smem_u32(smem + L::A_Q + L::T_BYTES), BM * 128, 1024);
+      const SDesc mO0 = sdesc_make(smem_u32(smem + L::A_DO), BM * 128, 1024);
+      const SDesc mO1 = sdesc_make(smem_u32(smem + L::A_DO + L::T_BYTES), BM * 128, 1024);
       auto issue_sdp = [&](int t) -> bool {
         const int s = t & 1;
         if (!mbar_wait(&q_full[s], (t >> 1) & 1, p.wc, abort_flag, SITE_BWD_MMA)) return false;
         tc_fence_after();
+        const SDesc bq = s ? kQ1 : kQ0;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K_j Q_t^T
           const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          umma_f16_ss(tS, sdesc_sw128(sK + off, 16, 1024),
-                      sdesc_sw128(sQ0 + s * L::T_BYTES + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+          umma_f16_ss(tS, sdesc_at(kK, off), sdesc_at(bq, off), id_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(s_full);
         if (!mbar_wait(&do_full[s], (t >> 1) & 1, p.wc, abort_flag, SITE_BWD_MMA)) return false;
         tc_fence_after();
+        const SDesc bo = s ? kO1 : kO0;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V_j dO_t^T
           const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          umma_f16_ss(tdP, sdesc_sw128(sV + off, 16, 1024),
-                      sdesc_sw128(sdO0 + s * L::T_BYTES + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+          umma_f16_ss(tdP, sdesc_at(kV, off), sdesc_at(bo, off), id_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(dp_full);
         return true;
@@ -287,16 +294,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after();
         // A operands from tensor memory: queries [64w, 64w+64) of P^T (dS^T)
         // sit packed in columns [64w, 64w+32) of the S^T (dP^T) region.
+        const SDesc bo = s ? mO1 : mO0, bq = s ? mQ1 : mQ0;
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)  // dV += P^T dO_t
-          umma_f16_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8,
-                      sdesc_sw128(sdO0 + s * L::T_BYTES + kk * 2048, BM * 128, 1024), id_kv,
+          umma_f16_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_at(bo, kk * 2048), id_kv,
                       (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&do_empty[s]);
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)  // dK += dS^T Q_t
-          umma_f16_ts(tdK, tdP + (kk >> 2) * 64 + (kk & 3) * 8,
-                      sdesc_sw128(sQ0 + s * L::T_BYTES + kk * 2048, BM * 128, 1024), id_kv,
+          umma_f16_ts(tdK, tdP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_at(bq, kk * 2048), id_kv,
                       (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&q_empty[s]);
         // next tile: S^T and dP^T overwrite the regions just read, after them
@@ -513,18 +519,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0);  // S, dP
       const uint32_t id_q = idesc_bf16_f32(BM, D, 0, 1);   // dQ (A in tensor memory)
-      const uint32_t sQ = smem_u32(smem + L::B_Q);
-      const uint32_t sdO = smem_u32(smem + L::B_DO);
-      const uint32_t sK0 = smem_u32(smem + L::B_K);
-      const uint32_t sV0 = smem_u32(smem + L::B_V);
+      const SDesc kQ = sdesc_make(smem_u32(smem + L::B_Q), 16, 1024);
+      const SDesc kdO = sdesc_make(smem_u32(smem + L::B_DO), 16, 1024);
+      const SDesc kK0 = sdesc_make(smem_u32(smem + L::B_K), 16, 1024);
+      const SDesc kK1 = sdesc_make(smem_u32(smem + L::B_K + L::T_BYTES), 16, 1024);
+      const SDesc kV0 = sdesc_make(smem_u32(smem + L::B_V), 16, 1024);
+      const SDesc kV1 = sdesc_make(smem_u32(smem + L::B_V + L::T_BYTES), 16, 1024);
+      const SDesc mK0 = sdesc_make(smem_u32(smem + L::B_K), BM * 128, 1024);
+      const SDesc mK1 = sdesc_make(smem_u32(smem + L::B_K + L::T_BYTES), BM * 128, 1024);
       auto issue_s = [&](int j) -> bool {  // S(j) = Q K_j^T into buffer j&1
         if (!mbar_wait(&k_full[j & 1], (j >> 1) & 1, p.wc, abort_flag, SITE_DQ_MMA)) return false;
         tc_fence_after();
+        const SDesc b = (j & 1) ? kK1 : kK0;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          umma_f16_ss(tmem + (j & 1) * 128, sdesc_sw128(sQ + off, 16, 1024),
-                      sdesc_sw128(sK0 + (j & 1) * L::T_BYTES + off, 16, 1024), id_s,
+          umma_f16_ss(tmem + (j & 1) * 128, sdesc_at(kQ, off), sdesc_at(b, off), id_s,
                       kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[j & 1]);
@@ -533,12 +543,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       auto issue_dp = [&](int j) -> bool {  // dP(j) = dO V_j^T
         if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, p.wc, abort_flag, SITE_DQ_MMA)) return false;
         tc_fence_after();
+        const SDesc b = (j & 1) ? kV1 : kV0;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          umma_f16_ss(tdP, sdesc_sw128(sdO + off, 16, 1024),
-                      sdesc_sw128(sV0 + (j & 1) * L::T_BYTES + off, 16, 1024), id_s,
-                      kk > 0 ? 1u : 0u);
+          umma_f16_ss(tdP, sdesc_at(kdO, off), sdesc_at(b, off), id_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(dp_full);
         umma_commit(&v_empty[j & 1]);  // V_j is read by dP(j) only
@@ -560,10 +569,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // dQ += dS(j) K_j: keys [64w, 64w+64) of dS sit packed in columns
         // [64w, 64w+32) of S buffer j&1
         const uint32_t tA = tmem + (j & 1) * 128;
+        const SDesc bk = (j & 1) ? mK1 : mK0;
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          umma_f16_ts(tdQ, tA + (kk >> 2) * 64 + (kk & 3) * 8,
-                      sdesc_sw128(sK0 + (j & 1) * L::T_BYTES + kk * 2048, BM * 128, 1024), id_q,
+          umma_f16_ts(tdQ, tA + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_at(bk, kk * 2048), id_q,
                       (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&k_empty[j & 1]);
         if (j + 1 < NJ && !issue_dp(j + 1)) {

@@ -212,30 +212,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       const uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
       const uint32_t idO = idesc_bf16_f32(BM, D, 0, 1);
-      const uint32_t sQ = smem_u32(smem + L::OFF_Q);
-      const uint32_t sK = smem_u32(smem + L::OFF_K);
-      const uint32_t sV = smem_u32(smem + L::OFF_V);
+      // Base descriptors built once; every MMA below only adds a
+      // compile-time byte offset to the low word.
+      const SDesc dQ0 = sdesc_make(smem_u32(smem + L::OFF_Q), 16, 1024);
+      const SDesc dQ1 = sdesc_make(smem_u32(smem + L::OFF_Q + L::Q_BYTES), 16, 1024);
+      const SDesc dK0 = sdesc_make(smem_u32(smem + L::OFF_K), 16, 1024);
+      const SDesc dK1 = sdesc_make(smem_u32(smem + L::OFF_K + L::KV_BYTES), 16, 1024);
+      const SDesc dV0 = sdesc_make(smem_u32(smem + L::OFF_V), BN * 128, 1024);
+      const SDesc dV1 = sdesc_make(smem_u32(smem + L::OFF_V + L::KV_BYTES), BN * 128, 1024);
+      static_assert(STAGES == 2, "descriptor selection assumes two stages");
       // S_t(j) = Q_t K_j^T into columns [128t, 128t+128)
       auto issue_s = [&](int t, int j) {
-        const int st = j % STAGES;
+        const SDesc a = t ? dQ1 : dQ0;
+        const SDesc b = (j & 1) ? dK1 : dK0;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          umma_f16_ss(tmem + t * BN, sdesc_sw128(sQ + t * L::Q_BYTES + off, 16, 1024),
-                      sdesc_sw128(sK + st * L::KV_BYTES + (kk >> 2) * (BN * 128) + (kk & 3) * 32,
-                                  16, 1024),
-                      idS, kk > 0 ? 1u : 0u);
+          umma_f16_ss(tmem + t * BN, sdesc_at(a, off), sdesc_at(b, off), idS, kk > 0 ? 1u : 0u);
         }
       };
       // O_t += P_hi V_j + P_lo V_j, P read from tensor memory
       auto issue_pv = [&](int t, int j) {
-        const int st = j % STAGES;
+        const SDesc b = (j & 1) ? dV1 : dV0;
+        const uint32_t tP = tmem + t * BN;
 #pragma unroll
         for (int part = 0; part < 2; ++part)
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            umma_f16_ts(tmem + 256 + t * 128, tmem + t * BN + kk * 16 + part * 8,
-                        sdesc_sw128(sV + st * L::KV_BYTES + kk * 2048, BN * 128, 1024), idO,
+            umma_f16_ts(tmem + 256 + t * 128, tP + kk * 16 + part * 8, sdesc_at(b, kk * 2048), idO,
                         (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(q_full, 0, p.wc, abort_flag, SITE_FWD_MMA) &&

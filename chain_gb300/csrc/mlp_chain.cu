@@ -171,8 +171,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       const uint32_t id1 = idesc_bf16_f32(BM, HC, 0, 1);  // T = X W1, W1 MN-major
       const uint32_t id2 = idesc_bf16_f32(BM, BP, 0, 1);  // O += H W2, W2 MN-major
+      // ring stage s: X tile (K-major) at 0, W1 (MN-major) at 16 KB; W2 tiles
+      // (MN-major) at 0.  Base descriptors built once per stage.
       const uint32_t ring = smem_u32(smem + L::OFF_RING);
-      const uint32_t sH[2] = {smem_u32(smem + L::OFF_HHI), smem_u32(smem + L::OFF_HLO)};
+      SDesc dX[NSTAGE], dW1[NSTAGE], dW2[NSTAGE];
+#pragma unroll
+      for (int q = 0; q < NSTAGE; ++q) {
+        dX[q] = sdesc_make(ring + q * STAGE_BYTES, 16, 1024);
+        dW1[q] = sdesc_make(ring + q * STAGE_BYTES + 16384, 8192, 1024);
+        dW2[q] = sdesc_make(ring + q * STAGE_BYTES, 8192, 1024);
+      }
+      const SDesc dHhi = sdesc_make(smem_u32(smem + L::OFF_HHI), 16, 1024);
+      const SDesc dHlo = sdesc_make(smem_u32(smem + L::OFF_HLO), 16, 1024);
       int st = 0;
       bool ok = true;
       for (int c = 0; c <= NC && ok; ++c) {
@@ -189,11 +199,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t base = ring + s * STAGE_BYTES;
+            SDesc ax = dX[0], bw = dW1[0];
+#pragma unroll
+            for (int q = 1; q < NSTAGE; ++q)
+              if (s == q) {
+                ax = dX[q];
+                bw = dW1[q];
+              }
 #pragma unroll
             for (int kk = 0; kk < KT / 16; ++kk)
-              umma_f16_ss(tmem + b * HC, sdesc_sw128(base + kk * 32, 16, 1024),
-                          sdesc_sw128(base + 16384 + kk * 2048, 8192, 1024), id1,
+              umma_f16_ss(tmem + b * HC, sdesc_at(ax, kk * 32), sdesc_at(bw, kk * 2048), id1,
                           (t > 0 || kk > 0) ? 1u : 0u);
             umma_commit(&empty[s]);
           }
@@ -213,13 +228,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t base = ring + s * STAGE_BYTES;
+            SDesc bw = dW2[0];
+#pragma unroll
+            for (int q = 1; q < NSTAGE; ++q)
+              if (s == q) bw = dW2[q];
 #pragma unroll
             for (int part = 0; part < 2; ++part)
 #pragma unroll
               for (int kk = 0; kk < KT / 16; ++kk)
-                umma_f16_ss(tmem + 256, sdesc_sw128(sH[part] + h * (BM * 128) + kk * 32, 16, 1024),
-                            sdesc_sw128(base + kk * 2048, 8192, 1024), id2,
+                umma_f16_ss(tmem + 256, sdesc_at(part ? dHlo : dHhi, h * (BM * 128) + kk * 32),
+                            sdesc_at(bw, kk * 2048), id2,
                             (cp > 0 || h > 0 || part > 0 || kk > 0) ? 1u : 0u);
             umma_commit(&empty[s]);
           }

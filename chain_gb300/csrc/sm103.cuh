@@ -249,6 +249,25 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same descriptor split into a 32-bit low word (start address, LBO) and
+// a constant high word (SBO, version, swizzle), so that the hot MMA loops
+// advance the start address with a single 32-bit add: the start-address
+// field never carries into the LBO field because shared-memory addresses
+// stay below 256 KB.
+struct SDesc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ SDesc sdesc_make(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  SDesc d;
+  d.lo = ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+  d.hi = ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+  return d;
+}
+// Descriptor of the tile starting byte_off bytes after the base.
+__device__ __forceinline__ uint64_t sdesc_at(const SDesc &d, uint32_t byte_off) {
+  return (static_cast<uint64_t>(d.hi) << 32) | static_cast<uint64_t>(d.lo + (byte_off >> 4));
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and f32 accumulator:
 //  [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B format,
 //  [15] A MN-major, [16] B MN-major, [17,23) N >> 3, [24,29) M >> 4.
