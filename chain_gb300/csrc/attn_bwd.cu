@@ -14,8 +14,10 @@
 //   bwd_dkdv   one CTA per (head, 128-key block j), looping over the query
 //              tiles i that see block j (i >= j when causal):
 //                S^T = K_j Q_i^T,  dP^T = V_j dO_i^T      (tensor memory)
-//                P^T, dS^T written back as bf16 over those columns
-//                dV += P^T dO_i,  dK += dS^T Q_i           (A from tensor memory)
+//                P^T as a bf16 tile in shared memory, which frees the S^T
+//                columns for S^T of the next tile at once;
+//                dS^T written back as bf16 over the dP^T columns
+//                dV += P^T dO_i (shared A),  dK += dS^T Q_i (tensor-memory A)
 //   bwd_dq     one CTA per (head, 128-query tile i), looping over the key
 //              tiles j <= i:
 //                S = Q_i K_j^T (two buffers),  dP = dO_i V_j^T
@@ -45,13 +47,14 @@ constexpr int NTHREADS = 320;
 template <int D>
 struct BwdLayout {
   static constexpr uint32_t T_BYTES = BM * D * 2;  // one [128][D] bf16 tile
-  // bwd_dkdv: K_j, V_j, Q (2 stages), dO (2 stages)
+  // bwd_dkdv: K_j, V_j, Q (2 stages), dO (2 stages), P^T
   static constexpr uint32_t A_K = 0;
   static constexpr uint32_t A_V = A_K + T_BYTES;
   static constexpr uint32_t A_Q = A_V + T_BYTES;
   static constexpr uint32_t A_DO = A_Q + 2 * T_BYTES;
-  static constexpr uint32_t A_LD = A_DO + 2 * T_BYTES;  // LSE/D staging [2 wg][2 buf][64] x2
-  static constexpr uint32_t A_BAR = A_LD + 2048;
+  static constexpr uint32_t A_PT = A_DO + 2 * T_BYTES;  // P^T [128 keys][128 queries] bf16
+  static constexpr uint32_t A_LD = A_PT + BM * BM * 2;  // LSE/D staging [2 wg][64] x2
+  static constexpr uint32_t A_BAR = A_LD + 1024;
   // bwd_dq: Q_i, dO_i once; K, V (2 stages each)
   static constexpr uint32_t B_Q = 0;
   static constexpr uint32_t B_DO = B_Q + T_BYTES;
@@ -170,13 +173,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t *do_empty = bars + 7;  // [2]
   uint64_t *s_full = bars + 9;
   uint64_t *dp_full = bars + 10;
-  uint64_t *p_ready = bars + 11;  // both compute warpgroups (256 arrivals)
+  uint64_t *p_ready = bars + 11;  // P^T in shared memory, dS^T in tensor memory (256 arrivals)
   uint64_t *fin = bars + 12;
   uint64_t *mma_drain = bars + 13;
+  uint64_t *s_free = bars + 14;   // S^T read into registers (256 arrivals)
+  uint64_t *pt_free = bars + 15;  // dV MMA done with the P^T tile
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::A_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::A_MISC + 4);
-  float *sL = reinterpret_cast<float *>(smem + L::A_LD);  // [wg][buf][64], LSE in log2 units
-  float *sDv = sL + 2 * 2 * 64;                            // [wg][buf][64]
+  float *sL = reinterpret_cast<float *>(smem + L::A_LD);  // [wg][64], LSE in log2 units
+  float *sDv = sL + 2 * 64;                                // [wg][64]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -188,7 +193,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int T = p.nb - i_begin;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < 14; ++b) mbar_init(&bars[b], &bars[b] == p_ready ? 256u : 1u);
+    for (int b = 0; b < 16; ++b)
+      mbar_init(&bars[b], (&bars[b] == p_ready || &bars[b] == s_free) ? 256u : 1u);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -248,12 +254,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncwarp();
   } else if (warp == 9) {
     // --------------------------------------------------------- MMA issuer
+    // Per query tile t, in issue (= execution) order:
+    //   S^T(t+1)                     once the warpgroups have read S^T(t)
+    //   dK += dS^T(t) Q_t            A from tensor memory
+    //   dV += P^T(t) dO_t            A from shared memory
+    //   dP^T(t+1)                    over dS^T(t), after dK(t) read it
+    // so the exponentials of tile t+1 overlap the products of tile t.
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0);  // S^T, dP^T
-      const uint32_t id_kv = idesc_bf16_f32(BM, D, 0, 1);  // dV, dK (A in tensor memory)
+      const uint32_t id_kv = idesc_bf16_f32(BM, D, 0, 1);  // dV, dK (B MN-major)
       // base descriptors, built once (K-major operands, then MN-major views)
       const SDesc kK = sdesc_make(smem_u32(smem + L::A_K), 16, 1024);
       const SDesc kV = sdesc_make(smem_u32(smem + L::A_V), 16, 1024);
+      const SDesc kP = sdesc_make(smem_u32(smem + L::A_PT), 16, 1024);
       const SDesc kQ0 = sdesc_make(smem_u32(smem + L::A_Q), 16, 1024);
       const SDesc kQ1 = sdesc_make(smem_u32(smem + L::A_Q + L::T_BYTES), 16, 1024);
       const SDesc kO0 = sdesc_make(smem_u32(smem + L::A_DO), 16, 1024);
@@ -262,51 +275,63 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const SDesc mQ1 = sdesc_make(smem_u32(smem + L::A_Q + L::T_BYTES), BM * 128, 1024);
       const SDesc mO0 = sdesc_make(smem_u32(smem + L::A_DO), BM * 128, 1024);
       const SDesc mO1 = sdesc_make(smem_u32(smem + L::A_DO + L::T_BYTES), BM * 128, 1024);
-      auto issue_sdp = [&](int t) -> bool {
+      auto issue_s = [&](int t) -> bool {  // S^T = K_j Q_t^T
         const int s = t & 1;
         if (!mbar_wait(&q_full[s], (t >> 1) & 1, p.wc, abort_flag, SITE_BWD_MMA)) return false;
         tc_fence_after();
         const SDesc bq = s ? kQ1 : kQ0;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K_j Q_t^T
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
           umma_f16_ss(tS, sdesc_at(kK, off), sdesc_at(bq, off), id_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(s_full);
+        return true;
+      };
+      auto issue_dp = [&](int t) -> bool {  // dP^T = V_j dO_t^T
+        const int s = t & 1;
         if (!mbar_wait(&do_full[s], (t >> 1) & 1, p.wc, abort_flag, SITE_BWD_MMA)) return false;
         tc_fence_after();
         const SDesc bo = s ? kO1 : kO0;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V_j dO_t^T
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
           umma_f16_ss(tdP, sdesc_at(kV, off), sdesc_at(bo, off), id_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(dp_full);
         return true;
       };
-      bool ok = mbar_wait(kv_full, 0, p.wc, abort_flag, SITE_BWD_MMA) && (T == 0 || issue_sdp(0));
+      bool ok = mbar_wait(kv_full, 0, p.wc, abort_flag, SITE_BWD_MMA) &&
+                (T == 0 || (issue_s(0) && issue_dp(0)));
       for (int t = 0; ok && t < T; ++t) {
         const int s = t & 1;
+        if (t + 1 < T) {
+          if (!mbar_wait(s_free, t & 1, p.wc, abort_flag, SITE_BWD_MMA) || !issue_s(t + 1)) {
+            ok = false;
+            break;
+          }
+        }
         if (!mbar_wait(p_ready, t & 1, p.wc, abort_flag, SITE_BWD_MMA)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // A operands from tensor memory: queries [64w, 64w+64) of P^T (dS^T)
-        // sit packed in columns [64w, 64w+32) of the S^T (dP^T) region.
-        const SDesc bo = s ? mO1 : mO0, bq = s ? mQ1 : mQ0;
+        // dS^T of queries [64w, 64w+64) sits packed in columns [64w, 64w+32)
+        // of the dP^T region
+        const SDesc bq = s ? mQ1 : mQ0;
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)  // dV += P^T dO_t
-          umma_f16_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_at(bo, kk * 2048), id_kv,
-                      (t > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&do_empty[s]);
-#pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)  // dK += dS^T Q_t
+        for (int kk = 0; kk < BM / 16; ++kk)
           umma_f16_ts(tdK, tdP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_at(bq, kk * 2048), id_kv,
                       (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&q_empty[s]);
-        // next tile: S^T and dP^T overwrite the regions just read, after them
-        if (t + 1 < T && !issue_sdp(t + 1)) {
+        const SDesc bo = s ? mO1 : mO0;
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          umma_f16_ss(tdV, sdesc_at(kP, (kk >> 2) * (BM * 128) + (kk & 3) * 32),
+                      sdesc_at(bo, kk * 2048), id_kv, (t > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&do_empty[s]);
+        umma_commit(pt_free);
+        if (t + 1 < T && !issue_dp(t + 1)) {
           ok = false;
           break;
         }
@@ -318,11 +343,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncwarp();
   } else {
     // --------------------------------------------- compute (two warpgroups)
+    // Every warp of a warpgroup passes the same named barriers: after a
+    // failed wait (ok false) the remaining waits are skipped, not the loop.
     const int w = warp >> 2;
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int kv_idx = jb * BM + r;
     const bool kv_ok = kv_idx < p.n;
+    // P^T row r, queries [64w, 64w+64): 128 bytes of a 128B-swizzled tile
+    const uint32_t pt_row = smem_u32(smem + L::A_PT + w * (BM * 128) + r * 128);
+    float *wl = sL + w * 64;
+    float *wd = sDv + w * 64;
     // LSE (log2 units) and D of query 64w + r of a tile (r < 64), fetched
     // one tile ahead
     auto fetch = [&](int i, float &lv, float &dv) {
@@ -334,30 +365,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float l_next = INFINITY, d_next = 0.0f;
     if (T > 0) fetch(i_begin, l_next, d_next);
     bool ok = true;
-    for (int t = 0; t < T && ok; ++t) {
-      const int i = i_begin + t, buf = t & 1;
+    for (int t = 0; t < T; ++t) {
+      const int i = i_begin + t;
       const bool diag = p.causal && (i == jb);
-      float *wl = sL + (w * 2 + buf) * 64;
-      float *wd = sDv + (w * 2 + buf) * 64;
+      if (t > 0) named_bar_sync(1 + w, 128);  // warpgroup done with the staged values of t-1
       if (r < 64) {
         wl[r] = l_next;
         wd[r] = d_next;
       }
-      if (t + 1 < T) fetch(i + 1, l_next, d_next);
       named_bar_sync(1 + w, 128);
-      if (!mbar_wait(s_full, t & 1, p.wc, abort_flag, SITE_BWD_COMPUTE)) {
-        ok = false;
-        break;
-      }
+      if (t + 1 < T) fetch(i + 1, l_next, d_next);
+      if (ok) ok = mbar_wait(s_full, t & 1, p.wc, abort_flag, SITE_BWD_COMPUTE);
       tc_fence_after();
-      // P^T for queries [64w, 64w+64): fp32 exponentials, bf16 pairs written
-      // back over the S^T columns just read
+      // P^T for queries [64w, 64w+64): fp32 exponentials; S^T is released
+      // to the next product as soon as it sits in registers
       float pf[64];
       {
         uint32_t sv[64];
         tmem_ld32(tS + lane_off + 64 * w, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
         tmem_ld32(tS + lane_off + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(s_free);
         const float4 *wl4 = reinterpret_cast<const float4 *>(wl);
 #pragma unroll
         for (int c4 = 0; c4 < 16; ++c4) {
@@ -371,15 +400,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             pf[qq] = pr;
           }
         }
+      }
+      {
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(pf[2 * c], pf[2 * c + 1]);
-        tmem_st32(tS + lane_off + 64 * w, pk);
+        // the dV product of tile t-1 still reads the P^T tile
+        if (ok && t > 0) ok = mbar_wait(pt_free, (t - 1) & 1, p.wc, abort_flag, SITE_BWD_COMPUTE);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          st_shared_v4(pt_row + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                       pk[4 * c + 3]);
+        fence_proxy_async_smem();
       }
-      if (!mbar_wait(dp_full, t & 1, p.wc, abort_flag, SITE_BWD_COMPUTE)) {
-        ok = false;
-        break;
-      }
+      if (ok) ok = mbar_wait(dp_full, t & 1, p.wc, abort_flag, SITE_BWD_COMPUTE);
       tc_fence_after();
       // dS^T = P^T o (dP^T - D) for the same queries, over the dP^T columns
       {
