@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int u = 0; u < 4; ++u) {
             const int qq = 4 * c4 + u;
             float pr = ex2(fmaf(__uint_as_float(sv[qq]), p.scale_log2, -ls[u]));
-            if (!kv_ok || (diag && 64 * w + qq < r)) pr = 0.0f;
+            if (!kv_ok || (diag && 64 * w + qq < r)) pr = 0.0f;  // a select, no branch
             pf[qq] = pr;
           }
         }
@@ -646,13 +646,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_ld32(tSb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          float pr = ex2(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lse2));
-          if (masked) {
+        for (int c = 0; c < 64; ++c) pf[c] = ex2(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lse2));
+        // keys after the query (diagonal tile) or beyond n (ragged tile): one
+        // branch around the whole pass, none in the loop above
+        if (masked) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
             const int kv = j * BM + 64 * w + c;
-            if ((p.causal && kv > q_idx) || kv >= p.n) pr = 0.0f;
+            if ((p.causal && kv > q_idx) || kv >= p.n) pf[c] = 0.0f;
           }
-          pf[c] = pr;
         }
       }
       if (!mbar_wait(dp_full, j & 1, p.wc, abort_flag, SITE_DQ_COMPUTE)) {
