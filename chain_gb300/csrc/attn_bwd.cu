@@ -19,9 +19,10 @@
 //                dS^T written back as bf16 over the dP^T columns
 //                dV += P^T dO_i (shared A),  dK += dS^T Q_i (tensor-memory A)
 //   bwd_dq     one CTA per (head, 128-query tile i), looping over the key
-//              tiles j <= i:
-//                S = Q_i K_j^T (two buffers),  dP = dO_i V_j^T
-//                dS written back as bf16 over the S columns
+//              tiles j <= i; Q_i and dO_i stay in tensor memory as the A
+//              operand of
+//                S = Q_i K_j^T,  dP = dO_i V_j^T
+//                dS written back as bf16 over the dP columns
 //                dQ += dS K_j                               (A from tensor memory)
 // bwd_dq recomputes S and dP, 7 products per tile pair instead of 5, in
 // exchange for accumulating dQ on chip instead of adding 128 x 128 fp32
@@ -55,13 +56,11 @@ struct BwdLayout {
   static constexpr uint32_t A_PT = A_DO + 2 * T_BYTES;  // P^T [128 keys][128 queries] bf16
   static constexpr uint32_t A_LD = A_PT + BM * BM * 2;  // LSE/D staging [2 wg][64] x2
   static constexpr uint32_t A_BAR = A_LD + 1024;
-  // bwd_dq: Q_i, dO_i once; K, V (2 stages each)
-  static constexpr uint32_t B_Q = 0;
-  static constexpr uint32_t B_DO = B_Q + T_BYTES;
-  static constexpr uint32_t B_K = B_DO + T_BYTES;
-  static constexpr uint32_t B_V = B_K + 2 * T_BYTES;
-  static constexpr uint32_t B_BAR = B_V + 2 * T_BYTES;
-  static constexpr uint32_t NBAR = 16;
+  // bwd_dq: K, V (3 stages each); Q_i, dO_i live in tensor memory
+  static constexpr uint32_t B_K = 0;
+  static constexpr uint32_t B_V = B_K + 3 * T_BYTES;
+  static constexpr uint32_t B_BAR = B_V + 3 * T_BYTES;
+  static constexpr uint32_t NBAR = 20;
   static constexpr uint32_t A_MISC = A_BAR + NBAR * 8;
   static constexpr uint32_t B_MISC = B_BAR + NBAR * 8;
   static constexpr uint32_t A_ALLOC =
@@ -75,6 +74,7 @@ struct BwdParams {
   float scale, scale_log2;
   const float *LSE;   // [BH][n]
   const float *Dvec;  // [BH][n]
+  const __nv_bfloat16 *Q, *dO;  // [BH][n][D]
   __nv_bfloat16 *dQ, *dK, *dV;
   WaitCfg wc;
 };
@@ -458,26 +458,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // ------------------------------------------------------------ dQ kernel
+// Q_i and dO_i are the same for every key tile of a CTA, so they sit in
+// tensor memory as the A operand of S = Q_i K_j^T and dP = dO_i V_j^T: those
+// products then read only K_j or V_j from shared memory.
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
-                  const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV,
-                  const __grid_constant__ CUtensorMap tmdO, const BwdParams p) {
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const BwdParams p) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::B_BAR);
-  uint64_t *qd_full = bars + 0;
-  uint64_t *k_full = bars + 1;   // [2]
-  uint64_t *k_empty = bars + 3;  // [2]
-  uint64_t *v_full = bars + 5;   // [2]
-  uint64_t *v_empty = bars + 7;  // [2]
-  uint64_t *s_full = bars + 9;   // [2]
-  uint64_t *dp_full = bars + 11;
-  uint64_t *p_ready = bars + 12;  // 256 arrivals
-  uint64_t *fin = bars + 13;
-  uint64_t *mma_drain = bars + 14;
+  uint64_t *k_full = bars + 0;    // [3]
+  uint64_t *k_empty = bars + 3;   // [3]
+  uint64_t *v_full = bars + 6;    // [3]
+  uint64_t *v_empty = bars + 9;   // [3]
+  uint64_t *qd_ready = bars + 12; // Q_i, dO_i in tensor memory (256 arrivals)
+  uint64_t *s_full = bars + 13;
+  uint64_t *s_free = bars + 14;   // S read into registers (256 arrivals)
+  uint64_t *dp_full = bars + 15;
+  uint64_t *p_ready = bars + 16;  // dS in tensor memory (256 arrivals)
+  uint64_t *fin = bars + 17;
+  uint64_t *mma_drain = bars + 18;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::B_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::B_MISC + 4);
 
@@ -489,7 +491,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int NJ = p.causal ? ib + 1 : p.nb;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < 15; ++b) mbar_init(&bars[b], &bars[b] == p_ready ? 256u : 1u);
+    for (int b = 0; b < 19; ++b) {
+      const bool wide = &bars[b] == qd_ready || &bars[b] == s_free || &bars[b] == p_ready;
+      mbar_init(&bars[b], wide ? 256u : 1u);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -498,125 +503,140 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tmem_relinquish();
   }
   if (warp == 8 && lane == 0) {
-    tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    tma_prefetch_desc(&tmdO);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // S buffers [0,128) and [128,256), dP [256,384), dQ [384, 384+D)
-  const uint32_t tdP = tmem + 256, tdQ = tmem + 384;
+  // S [0,128), dP / dS [128,256), dQ [256, 256+D), Q_i and dO_i as packed
+  // bf16 pairs (D/2 columns each) after it
+  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+  const uint32_t tQ = tmem + 256 + D, tdO = tmem + 256 + D + D / 2;
 
   if (warp == 8) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       int k_issued = 0, v_issued = 0;
-      mbar_arrive_expect_tx(qd_full, 2 * L::T_BYTES);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(smem + L::B_Q + c * (BM * 128), &tmQ, qd_full, c * 64, ib * BM, bh);
-        tma_load_3d(smem + L::B_DO + c * (BM * 128), &tmdO, qd_full, c * 64, ib * BM, bh);
-      }
       for (int j = 0; j < NJ; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(&k_empty[s], ((j >> 1) - 1) & 1, p.wc, abort_flag, SITE_DQ_PROD))
+        const int sk = j % 3;
+        if (j >= 3 && !mbar_wait(&k_empty[sk], ((j / 3) - 1) & 1, p.wc, abort_flag, SITE_DQ_PROD))
           break;
-        mbar_arrive_expect_tx(&k_full[s], L::T_BYTES);
+        mbar_arrive_expect_tx(&k_full[sk], L::T_BYTES);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + L::B_K + s * L::T_BYTES + c * (BM * 128), &tmK, &k_full[s], c * 64,
+          tma_load_3d(smem + L::B_K + sk * L::T_BYTES + c * (BM * 128), &tmK, &k_full[sk], c * 64,
                       j * BM, bh);
         k_issued = j + 1;
-        if (j >= 2 && !mbar_wait(&v_empty[s], ((j >> 1) - 1) & 1, p.wc, abort_flag, SITE_DQ_PROD))
+        if (j >= 3 && !mbar_wait(&v_empty[sk], ((j / 3) - 1) & 1, p.wc, abort_flag, SITE_DQ_PROD))
           break;
-        mbar_arrive_expect_tx(&v_full[s], L::T_BYTES);
+        mbar_arrive_expect_tx(&v_full[sk], L::T_BYTES);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + L::B_V + s * L::T_BYTES + c * (BM * 128), &tmV, &v_full[s], c * 64,
+          tma_load_3d(smem + L::B_V + sk * L::T_BYTES + c * (BM * 128), &tmV, &v_full[sk], c * 64,
                       j * BM, bh);
         v_issued = j + 1;
       }
       if (*abort_flag) {
-        drain_wait(qd_full, 0, p.wc);
-        for (int j = (k_issued > 2 ? k_issued - 2 : 0); j < k_issued; ++j)
-          drain_wait(&k_full[j & 1], (j >> 1) & 1, p.wc);
-        for (int j = (v_issued > 2 ? v_issued - 2 : 0); j < v_issued; ++j)
-          drain_wait(&v_full[j & 1], (j >> 1) & 1, p.wc);
+        for (int j = (k_issued > 3 ? k_issued - 3 : 0); j < k_issued; ++j)
+          drain_wait(&k_full[j % 3], (j / 3) & 1, p.wc);
+        for (int j = (v_issued > 3 ? v_issued - 3 : 0); j < v_issued; ++j)
+          drain_wait(&v_full[j % 3], (j / 3) & 1, p.wc);
       }
     }
     __syncwarp();
   } else if (warp == 9) {
     // --------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0);  // S, dP
-      const uint32_t id_q = idesc_bf16_f32(BM, D, 0, 1);   // dQ (A in tensor memory)
-      const SDesc kQ = sdesc_make(smem_u32(smem + L::B_Q), 16, 1024);
-      const SDesc kdO = sdesc_make(smem_u32(smem + L::B_DO), 16, 1024);
+    // Per key tile j, in issue (= execution) order:
+    //   S(j+1)           once the warpgroups hold S(j) in registers
+    //   dQ += dS(j) K_j  A from the dP columns
+    //   dP(j+1)          over dS(j), after dQ(j) read it
+    // The whole warp runs the loop; one elected lane issues each group and
+    // its commits.
+    {
+      const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0);  // S, dP (B K-major)
+      const uint32_t id_q = idesc_bf16_f32(BM, D, 0, 1);   // dQ (B MN-major)
       const SDesc kK0 = sdesc_make(smem_u32(smem + L::B_K), 16, 1024);
       const SDesc kK1 = sdesc_make(smem_u32(smem + L::B_K + L::T_BYTES), 16, 1024);
+      const SDesc kK2 = sdesc_make(smem_u32(smem + L::B_K + 2 * L::T_BYTES), 16, 1024);
       const SDesc kV0 = sdesc_make(smem_u32(smem + L::B_V), 16, 1024);
       const SDesc kV1 = sdesc_make(smem_u32(smem + L::B_V + L::T_BYTES), 16, 1024);
+      const SDesc kV2 = sdesc_make(smem_u32(smem + L::B_V + 2 * L::T_BYTES), 16, 1024);
       const SDesc mK0 = sdesc_make(smem_u32(smem + L::B_K), BM * 128, 1024);
       const SDesc mK1 = sdesc_make(smem_u32(smem + L::B_K + L::T_BYTES), BM * 128, 1024);
-      auto issue_s = [&](int j) -> bool {  // S(j) = Q K_j^T into buffer j&1
-        if (!mbar_wait(&k_full[j & 1], (j >> 1) & 1, p.wc, abort_flag, SITE_DQ_MMA)) return false;
+      const SDesc mK2 = sdesc_make(smem_u32(smem + L::B_K + 2 * L::T_BYTES), BM * 128, 1024);
+      auto issue_s = [&](int j) -> bool {  // S(j) = Q_i K_j^T
+        const int sk = j % 3;
+        if (!mbar_wait_warp(&k_full[sk], (j / 3) & 1, p.wc, abort_flag, SITE_DQ_MMA)) return false;
         tc_fence_after();
-        const SDesc b = (j & 1) ? kK1 : kK0;
+        const SDesc b = sk == 0 ? kK0 : (sk == 1 ? kK1 : kK2);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          umma_f16_ss(tmem + (j & 1) * 128, sdesc_at(kQ, off), sdesc_at(b, off), id_s,
-                      kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+            umma_f16_ts(tS, tQ + kk * 8, sdesc_at(b, off), id_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full);
         }
-        umma_commit(&s_full[j & 1]);
+        __syncwarp();
         return true;
       };
-      auto issue_dp = [&](int j) -> bool {  // dP(j) = dO V_j^T
-        if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, p.wc, abort_flag, SITE_DQ_MMA)) return false;
+      auto issue_dp = [&](int j) -> bool {  // dP(j) = dO_i V_j^T
+        const int sv = j % 3;
+        if (!mbar_wait_warp(&v_full[sv], (j / 3) & 1, p.wc, abort_flag, SITE_DQ_MMA)) return false;
         tc_fence_after();
-        const SDesc b = (j & 1) ? kV1 : kV0;
+        const SDesc b = sv == 0 ? kV0 : (sv == 1 ? kV1 : kV2);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          umma_f16_ss(tdP, sdesc_at(kdO, off), sdesc_at(b, off), id_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+            umma_f16_ts(tdP, tdO + kk * 8, sdesc_at(b, off), id_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(dp_full);
+          umma_commit(&v_empty[sv]);  // V_j is read by dP(j) only
         }
-        umma_commit(dp_full);
-        umma_commit(&v_empty[j & 1]);  // V_j is read by dP(j) only
+        __syncwarp();
         return true;
       };
-      bool ok = mbar_wait(qd_full, 0, p.wc, abort_flag, SITE_DQ_MMA) && issue_s(0) && issue_dp(0);
+      bool ok = mbar_wait_warp(qd_ready, 0, p.wc, abort_flag, SITE_DQ_MMA);
+      if (ok) tc_fence_after();
+      ok = ok && issue_s(0) && issue_dp(0);
       for (int j = 0; ok && j < NJ; ++j) {
-        // S(j+1) into the other buffer while the warpgroups work on tile j;
-        // that buffer's dS(j-1) was consumed by dQ(j-1), issued earlier
-        if (j + 1 < NJ && !issue_s(j + 1)) {
-          ok = false;
-          break;
+        if (j + 1 < NJ) {
+          if (!mbar_wait_warp(s_free, j & 1, p.wc, abort_flag, SITE_DQ_MMA) || !issue_s(j + 1)) {
+            ok = false;
+            break;
+          }
         }
-        if (!mbar_wait(p_ready, j & 1, p.wc, abort_flag, SITE_DQ_MMA)) {
+        if (!mbar_wait_warp(p_ready, j & 1, p.wc, abort_flag, SITE_DQ_MMA)) {
           ok = false;
           break;
         }
         tc_fence_after();
         // dQ += dS(j) K_j: keys [64w, 64w+64) of dS sit packed in columns
-        // [64w, 64w+32) of S buffer j&1
-        const uint32_t tA = tmem + (j & 1) * 128;
-        const SDesc bk = (j & 1) ? mK1 : mK0;
+        // [64w, 64w+32) of the dP region
+        const int sk = j % 3;
+        const SDesc bk = sk == 0 ? mK0 : (sk == 1 ? mK1 : mK2);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          umma_f16_ts(tdQ, tA + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_at(bk, kk * 2048), id_q,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&k_empty[j & 1]);
+          for (int kk = 0; kk < BM / 16; ++kk)
+            umma_f16_ts(tdQ, tdP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_at(bk, kk * 2048), id_q,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&k_empty[sk]);
+        }
+        __syncwarp();
         if (j + 1 < NJ && !issue_dp(j + 1)) {
           ok = false;
           break;
         }
       }
-      if (ok) umma_commit(fin);
-      umma_commit(mma_drain);
-      drain_wait(mma_drain, 0, p.wc);
+      if (elect_one()) {
+        if (ok) umma_commit(fin);
+        umma_commit(mma_drain);
+      }
+      __syncwarp();
+      if (lane == 0) drain_wait(mma_drain, 0, p.wc);
     }
     __syncwarp();
   } else {
@@ -630,11 +650,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const bool q_ok = q_idx < p.n;
     const float lse2 = q_ok ? p.LSE[(int64_t)bh * p.n + q_idx] * 1.4426950408889634f : INFINITY;
     const float dval = q_ok ? p.Dvec[(int64_t)bh * p.n + q_idx] : 0.0f;
+    // warpgroup 0 puts row q_idx of Q into tensor memory, warpgroup 1 the
+    // same row of dO (zeros past n); the bf16 pairs of a row are already
+    // the packed column words
+    {
+      const uint4 *src = reinterpret_cast<const uint4 *>((w ? p.dO : p.Q) +
+                                                         ((int64_t)bh * p.n + q_idx) * D);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t v[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 u = q_ok ? __ldg(src + c * 8 + k) : make_uint4(0u, 0u, 0u, 0u);
+          v[4 * k] = u.x;
+          v[4 * k + 1] = u.y;
+          v[4 * k + 2] = u.z;
+          v[4 * k + 3] = u.w;
+        }
+        tmem_st32((w ? tdO : tQ) + lane_off + 32 * c, v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(qd_ready);
+    }
     bool ok = true;
     for (int j = 0; j < NJ; ++j) {
       const bool masked = (p.causal && j == ib) || ((j + 1) * BM > p.n);
-      const uint32_t tSb = tmem + (j & 1) * 128 + lane_off + 64 * w;
-      if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, p.wc, abort_flag, SITE_DQ_COMPUTE)) {
+      if (!mbar_wait(s_full, j & 1, p.wc, abort_flag, SITE_DQ_COMPUTE)) {
         ok = false;
         break;
       }
@@ -642,9 +684,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       float pf[64];
       {
         uint32_t sv[64];
-        tmem_ld32(tSb, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_ld32(tSb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_ld32(tS + lane_off + 64 * w, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(tS + lane_off + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(s_free);  // S(j+1) may overwrite these columns
 #pragma unroll
         for (int c = 0; c < 64; ++c) pf[c] = ex2(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lse2));
         // keys after the query (diagonal tile) or beyond n (ragged tile): one
@@ -672,7 +716,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int c = 0; c < 32; ++c)
           ds[c] = pack_bf16(pf[2 * c] * (__uint_as_float(dp[2 * c]) - dval),
                             pf[2 * c + 1] * (__uint_as_float(dp[2 * c + 1]) - dval));
-        tmem_st32(tSb, ds);
+        // dS over the first half of the dP columns this warpgroup just read
+        tmem_st32(tdP + lane_off + 64 * w, ds);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -725,6 +770,8 @@ cudaError_t launch_bwd_d(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t s
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.LSE = a.LSE;
   p.Dvec = a.Dvec;
+  p.Q = static_cast<const __nv_bfloat16 *>(a.Q);
+  p.dO = static_cast<const __nv_bfloat16 *>(a.dO);
   p.dQ = static_cast<__nv_bfloat16 *>(a.dQ);
   p.dK = static_cast<__nv_bfloat16 *>(a.dK);
   p.dV = static_cast<__nv_bfloat16 *>(a.dV);
@@ -740,7 +787,7 @@ cudaError_t launch_bwd_d(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t s
   ka<<<grid, NTHREADS, L::A_ALLOC, st>>>(mq, mk, mv, mdo, p);
   timing_mark(st, 1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  kb<<<grid, NTHREADS, L::B_ALLOC, st>>>(mq, mk, mv, mdo, p);
+  kb<<<grid, NTHREADS, L::B_ALLOC, st>>>(mk, mv, p);
   timing_mark(st, 2);
   return cudaGetLastError();
 }

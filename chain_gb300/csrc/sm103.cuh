@@ -99,6 +99,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
   }
 }
 
+// Whole-warp form of mbar_wait: lane 0 waits, the warp shares the result.
+// Tensor-core issuers run as a whole converged warp and let one elected
+// lane issue (elect_one): a lone-lane issue loop loses most of its issue
+// slots to busy neighbour warps on the same scheduler.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, const WaitCfg &wc,
+                                               volatile int *abort, int site) {
+  int ok = 0;
+  if (lane_id() == 0) ok = mbar_wait(bar, parity, wc, abort, site) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// True in exactly one lane of a converged warp (the lowest active lane).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
