@@ -259,8 +259,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     //   dK += dS^T(t) Q_t            A from tensor memory
     //   dV += P^T(t) dO_t            A from shared memory
     //   dP^T(t+1)                    over dS^T(t), after dK(t) read it
-    // so the exponentials of tile t+1 overlap the products of tile t.
-    if (lane == 0) {
+    // so the exponentials of tile t+1 overlap the products of tile t.  The
+    // whole warp runs the loop; one elected lane issues each group and its
+    // commits.
+    {
       const uint32_t id_s = idesc_bf16_f32(BM, BM, 0, 0);  // S^T, dP^T
       const uint32_t id_kv = idesc_bf16_f32(BM, D, 0, 1);  // dV, dK (B MN-major)
       // base descriptors, built once (K-major operands, then MN-major views)
@@ -277,41 +279,47 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const SDesc mO1 = sdesc_make(smem_u32(smem + L::A_DO + L::T_BYTES), BM * 128, 1024);
       auto issue_s = [&](int t) -> bool {  // S^T = K_j Q_t^T
         const int s = t & 1;
-        if (!mbar_wait(&q_full[s], (t >> 1) & 1, p.wc, abort_flag, SITE_BWD_MMA)) return false;
+        if (!mbar_wait_warp(&q_full[s], (t >> 1) & 1, p.wc, abort_flag, SITE_BWD_MMA)) return false;
         tc_fence_after();
         const SDesc bq = s ? kQ1 : kQ0;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          umma_f16_ss(tS, sdesc_at(kK, off), sdesc_at(bq, off), id_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+            umma_f16_ss(tS, sdesc_at(kK, off), sdesc_at(bq, off), id_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full);
         }
-        umma_commit(s_full);
+        __syncwarp();
         return true;
       };
       auto issue_dp = [&](int t) -> bool {  // dP^T = V_j dO_t^T
         const int s = t & 1;
-        if (!mbar_wait(&do_full[s], (t >> 1) & 1, p.wc, abort_flag, SITE_BWD_MMA)) return false;
+        if (!mbar_wait_warp(&do_full[s], (t >> 1) & 1, p.wc, abort_flag, SITE_BWD_MMA)) return false;
         tc_fence_after();
         const SDesc bo = s ? kO1 : kO0;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          umma_f16_ss(tdP, sdesc_at(kV, off), sdesc_at(bo, off), id_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+            umma_f16_ss(tdP, sdesc_at(kV, off), sdesc_at(bo, off), id_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(dp_full);
         }
-        umma_commit(dp_full);
+        __syncwarp();
         return true;
       };
-      bool ok = mbar_wait(kv_full, 0, p.wc, abort_flag, SITE_BWD_MMA) &&
+      bool ok = mbar_wait_warp(kv_full, 0, p.wc, abort_flag, SITE_BWD_MMA) &&
                 (T == 0 || (issue_s(0) && issue_dp(0)));
       for (int t = 0; ok && t < T; ++t) {
         const int s = t & 1;
         if (t + 1 < T) {
-          if (!mbar_wait(s_free, t & 1, p.wc, abort_flag, SITE_BWD_MMA) || !issue_s(t + 1)) {
+          if (!mbar_wait_warp(s_free, t & 1, p.wc, abort_flag, SITE_BWD_MMA) || !issue_s(t + 1)) {
             ok = false;
             break;
           }
         }
-        if (!mbar_wait(p_ready, t & 1, p.wc, abort_flag, SITE_BWD_MMA)) {
+        if (!mbar_wait_warp(p_ready, t & 1, p.wc, abort_flag, SITE_BWD_MMA)) {
           ok = false;
           break;
         }
@@ -319,26 +327,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // dS^T of queries [64w, 64w+64) sits packed in columns [64w, 64w+32)
         // of the dP^T region
         const SDesc bq = s ? mQ1 : mQ0;
-#pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          umma_f16_ts(tdK, tdP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_at(bq, kk * 2048), id_kv,
-                      (t > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&q_empty[s]);
         const SDesc bo = s ? mO1 : mO0;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          umma_f16_ss(tdV, sdesc_at(kP, (kk >> 2) * (BM * 128) + (kk & 3) * 32),
-                      sdesc_at(bo, kk * 2048), id_kv, (t > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&do_empty[s]);
-        umma_commit(pt_free);
+          for (int kk = 0; kk < BM / 16; ++kk)
+            umma_f16_ts(tdK, tdP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_at(bq, kk * 2048), id_kv,
+                        (t > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&q_empty[s]);
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk)
+            umma_f16_ss(tdV, sdesc_at(kP, (kk >> 2) * (BM * 128) + (kk & 3) * 32),
+                        sdesc_at(bo, kk * 2048), id_kv, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&do_empty[s]);
+          umma_commit(pt_free);
+        }
+        __syncwarp();
         if (t + 1 < T && !issue_dp(t + 1)) {
           ok = false;
           break;
         }
       }
-      if (ok) umma_commit(fin);
-      umma_commit(mma_drain);
-      drain_wait(mma_drain, 0, p.wc);
+      if (elect_one()) {
+        if (ok) umma_commit(fin);
+        umma_commit(mma_drain);
+      }
+      __syncwarp();
+      if (lane == 0) drain_wait(mma_drain, 0, p.wc);
     }
     __syncwarp();
   } else {

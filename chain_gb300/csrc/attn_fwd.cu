@@ -209,7 +209,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncwarp();
   } else if (warp == 9) {
     // --------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop; one elected lane issues each group of
+    // products together with its commits.
+    {
       const uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
       const uint32_t idO = idesc_bf16_f32(BM, D, 0, 1);
       // Base descriptors built once; every MMA below only adds a
@@ -242,48 +244,64 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             umma_f16_ts(tmem + 256 + t * 128, tP + kk * 16 + part * 8, sdesc_at(b, kk * 2048), idO,
                         (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
       };
-      bool ok = mbar_wait(q_full, 0, p.wc, abort_flag, SITE_FWD_MMA) &&
-                mbar_wait(&k_full[0], 0, p.wc, abort_flag, SITE_FWD_MMA);
+      bool ok = mbar_wait_warp(q_full, 0, p.wc, abort_flag, SITE_FWD_MMA) &&
+                mbar_wait_warp(&k_full[0], 0, p.wc, abort_flag, SITE_FWD_MMA);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
-        umma_commit(&s_full[0]);
-        issue_s(1, 0);
-        umma_commit(&s_full[1]);
-        umma_commit(&k_empty[0]);
+        if (elect_one()) {
+          issue_s(0, 0);
+          umma_commit(&s_full[0]);
+          issue_s(1, 0);
+          umma_commit(&s_full[1]);
+          umma_commit(&k_empty[0]);
+        }
+        __syncwarp();
       }
       for (int j = 0; ok && j < nkv_b; ++j) {
         const int st = j % STAGES;
         const int jn = j + 1, stn = jn % STAGES;
-        if (!mbar_wait(&v_full[st], (j / STAGES) & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
+        if (!mbar_wait_warp(&v_full[st], (j / STAGES) & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
         if (j < nkv_a) {
-          if (!mbar_wait(&p_ready[0], j & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
+          if (!mbar_wait_warp(&p_ready[0], j & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
           tc_fence_after();
-          issue_pv(0, j);
-          umma_commit(&pv_done[0]);
+          if (elect_one()) {
+            issue_pv(0, j);
+            umma_commit(&pv_done[0]);
+          }
+          __syncwarp();
           if (jn < nkv_a) {
-            if (!mbar_wait(&k_full[stn], (jn / STAGES) & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
+            if (!mbar_wait_warp(&k_full[stn], (jn / STAGES) & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
             tc_fence_after();
-            issue_s(0, jn);
-            umma_commit(&s_full[0]);
+            if (elect_one()) {
+              issue_s(0, jn);
+              umma_commit(&s_full[0]);
+            }
+            __syncwarp();
           }
         }
-        if (!mbar_wait(&p_ready[1], j & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
+        if (!mbar_wait_warp(&p_ready[1], j & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
         tc_fence_after();
-        issue_pv(1, j);
-        umma_commit(&pv_done[1]);
-        umma_commit(&v_empty[st]);
+        if (elect_one()) {
+          issue_pv(1, j);
+          umma_commit(&pv_done[1]);
+          umma_commit(&v_empty[st]);
+        }
+        __syncwarp();
         if (jn < nkv_b) {
-          if (!mbar_wait(&k_full[stn], (jn / STAGES) & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
+          if (!mbar_wait_warp(&k_full[stn], (jn / STAGES) & 1, p.wc, abort_flag, SITE_FWD_MMA)) break;
           tc_fence_after();
-          issue_s(1, jn);
-          umma_commit(&s_full[1]);
-          umma_commit(&k_empty[stn]);
+          if (elect_one()) {
+            issue_s(1, jn);
+            umma_commit(&s_full[1]);
+            umma_commit(&k_empty[stn]);
+          }
+          __syncwarp();
         }
       }
       // No MMA may still be running when tensor memory is released.
-      umma_commit(mma_drain);
-      drain_wait(mma_drain, 0, p.wc);
+      if (elect_one()) umma_commit(mma_drain);
+      __syncwarp();
+      if (lane == 0) drain_wait(mma_drain, 0, p.wc);
     }
     __syncwarp();
   } else {

@@ -168,7 +168,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop; one elected lane issues each group of
+    // products together with its commits.
+    {
       const uint32_t id1 = idesc_bf16_f32(BM, HC, 0, 1);  // T = X W1, W1 MN-major
       const uint32_t id2 = idesc_bf16_f32(BM, BP, 0, 1);  // O += H W2, W2 MN-major
       // ring stage s: X tile (K-major) at 0, W1 (MN-major) at 16 KB; W2 tiles
@@ -188,13 +190,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int c = 0; c <= NC && ok; ++c) {
         if (c < NC) {
           const int b = c & 1;
-          if (c >= 2 && !mbar_wait(&t_free[b], ((c >> 1) - 1) & 1, p.wc, abort_flag, SITE_MLP_MMA)) {
+          if (c >= 2 && !mbar_wait_warp(&t_free[b], ((c >> 1) - 1) & 1, p.wc, abort_flag, SITE_MLP_MMA)) {
             ok = false;
             break;
           }
           for (int t = 0; t < NKT; ++t, ++st) {
             const int s = st % NSTAGE;
-            if (!mbar_wait(&full[s], (st / NSTAGE) & 1, p.wc, abort_flag, SITE_MLP_MMA)) {
+            if (!mbar_wait_warp(&full[s], (st / NSTAGE) & 1, p.wc, abort_flag, SITE_MLP_MMA)) {
               ok = false;
               break;
             }
@@ -206,24 +208,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 ax = dX[q];
                 bw = dW1[q];
               }
+            if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < KT / 16; ++kk)
-              umma_f16_ss(tmem + b * HC, sdesc_at(ax, kk * 32), sdesc_at(bw, kk * 2048), id1,
-                          (t > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&empty[s]);
+              for (int kk = 0; kk < KT / 16; ++kk)
+                umma_f16_ss(tmem + b * HC, sdesc_at(ax, kk * 32), sdesc_at(bw, kk * 2048), id1,
+                            (t > 0 || kk > 0) ? 1u : 0u);
+              umma_commit(&empty[s]);
+            }
+            __syncwarp();
           }
           if (!ok) break;
-          umma_commit(&t_full[b]);
+          if (elect_one()) umma_commit(&t_full[b]);
+          __syncwarp();
         }
         if (c >= 1) {
           const int cp = c - 1;
-          if (!mbar_wait(h_ready, cp & 1, p.wc, abort_flag, SITE_MLP_MMA)) {
+          if (!mbar_wait_warp(h_ready, cp & 1, p.wc, abort_flag, SITE_MLP_MMA)) {
             ok = false;
             break;
           }
           for (int h = 0; h < HC / KT; ++h, ++st) {
             const int s = st % NSTAGE;
-            if (!mbar_wait(&full[s], (st / NSTAGE) & 1, p.wc, abort_flag, SITE_MLP_MMA)) {
+            if (!mbar_wait_warp(&full[s], (st / NSTAGE) & 1, p.wc, abort_flag, SITE_MLP_MMA)) {
               ok = false;
               break;
             }
@@ -232,22 +238,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int q = 1; q < NSTAGE; ++q)
               if (s == q) bw = dW2[q];
+            if (elect_one()) {
 #pragma unroll
-            for (int part = 0; part < 2; ++part)
+              for (int part = 0; part < 2; ++part)
 #pragma unroll
-              for (int kk = 0; kk < KT / 16; ++kk)
-                umma_f16_ss(tmem + 256, sdesc_at(part ? dHlo : dHhi, h * (BM * 128) + kk * 32),
-                            sdesc_at(bw, kk * 2048), id2,
-                            (cp > 0 || h > 0 || part > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&empty[s]);
+                for (int kk = 0; kk < KT / 16; ++kk)
+                  umma_f16_ss(tmem + 256, sdesc_at(part ? dHlo : dHhi, h * (BM * 128) + kk * 32),
+                              sdesc_at(bw, kk * 2048), id2,
+                              (cp > 0 || h > 0 || part > 0 || kk > 0) ? 1u : 0u);
+              umma_commit(&empty[s]);
+            }
+            __syncwarp();
           }
           if (!ok) break;
-          umma_commit(h_free);
+          if (elect_one()) umma_commit(h_free);
+          __syncwarp();
         }
       }
-      if (ok) umma_commit(o_done);
-      umma_commit(mma_drain);
-      drain_wait(mma_drain, 0, p.wc);
+      if (elect_one()) {
+        if (ok) umma_commit(o_done);
+        umma_commit(mma_drain);
+      }
+      __syncwarp();
+      if (lane == 0) drain_wait(mma_drain, 0, p.wc);
     }
     __syncwarp();
   } else {
