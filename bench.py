@@ -420,6 +420,55 @@ def run_reference(args):
     return 0
 
 
+def measure_sp_fused(hp, reps=5):
+    """The relayout fused into the attention (chain_fwd_sp: Q, K, V read from
+    the sequence shards, O written back into them) against the unfused
+    sequence sp_relayout x3 + chain_fwd + sp_relayout_inverse, on the Ulysses
+    workload.  Measured beside the step, not part of its value."""
+    torch, cg, u = hp.torch, hp.cg, hp.u
+    Hl, N, d = u["H"] // u["p"], u["p"] * u["n_loc"], u["d"]
+    o_sh = torch.zeros_like(hp.shards[0])
+    l_sh = torch.empty(Hl, N, dtype=torch.float32, device=hp.dev)
+    scale = d ** -0.5
+
+    def fused():
+        cg.chain_fwd_sp(hp.shards[0], hp.shards[1], hp.shards[2], u["p"], u["g"], cg.MASK_CAUSAL,
+                        scale, o_sh, l_sh)
+
+    def unfused():
+        for t in range(3):
+            cg.sp_relayout(hp.shards[t], u["p"], u["g"], hp.hm[t])
+        cg.chain_fwd(hp.hm[0], hp.hm[1], hp.hm[2], cg.F_SOFTMAX, cg.MASK_CAUSAL, scale, hp.o4, hp.l4)
+        cg.sp_relayout_inverse(hp.o4, u["p"], u["g"], o_sh)
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return sorted(ts)[len(ts) // 2]
+
+    ms_f, ms_u = timed(fused), timed(unfused)
+    rc, site = cg.chain_check()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} site {site:#x} in the fused relayout measurement")
+    fl = attn_fwd_flops(Hl, N, d, True)
+    del o_sh, l_sh
+    return {"attn_fwd_sp_fused_8x131072x128": {
+        "ms": round(ms_f, 4), "TFLOPs": round(fl / (ms_f * 1e-3) / 1e12, 1),
+        "unfused_ms": round(ms_u, 4),
+        "unfused": "sp_relayout x3 + chain_fwd + sp_relayout_inverse",
+        "hbm_bytes_saved": 4 * 2 * Hl * N * d * 2,
+        "timing": f"median of {reps} after 2 warm-ups; inputs larger than L2"}}
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -600,6 +649,11 @@ def main():
             raise RuntimeError(f"device status {rc} site {site:#x} in e2e region")
         del hps
 
+    # ---- NEXT rows, measured beside the step (not part of its value)
+    nxt = None
+    if hp.shards[0].numel() and (args.only is None or "sp" in args.only):
+        nxt = measure_sp_fused(hp)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         v, s, desc, thr = oracle_sample()
@@ -616,7 +670,7 @@ def main():
                            "flops_per_step": hp.flops,
                            "frac_of_measured_peak": round(value / world / tf_peak, 4)},
                 "roofline": roof, "components": components, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": hp.launches * args.steps, "clocks": clocks}
+                "gpu_launches": hp.launches * args.steps, "clocks": clocks, "next_rows": nxt}
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()

@@ -70,6 +70,7 @@ def _load():
             lib.chain_bwd_noalloc.argtypes = [P, P, P, P, P, P, ci, ci, fl, P, P, P, vp]
             lib.chain_bwd_workspace_size.argtypes = [P, P]
             lib.chain_bwd_workspace_size.restype = ctypes.c_size_t
+            lib.chain_fwd_sp.argtypes = [P, P, P, ci, ci, ci, fl, P, P, vp]
             lib.sp_relayout.argtypes = [P, ci, ci, P, vp]
             lib.sp_relayout_inverse.argtypes = [P, ci, ci, P, vp]
             lib.chain_check.argtypes = [vp, ctypes.POINTER(ci)]
@@ -81,7 +82,8 @@ def _load():
             lib.chain_umma_selftest.argtypes = [vp, vp, vp, ci, ci, ci, vp]
             lib.chain_status_string.argtypes = [ci]
             lib.chain_status_string.restype = ctypes.c_char_p
-            for fn in ("chain_fwd", "chain_bwd", "chain_bwd_noalloc", "sp_relayout", "sp_relayout_inverse",
+            for fn in ("chain_fwd", "chain_fwd_sp", "chain_bwd", "chain_bwd_noalloc", "sp_relayout",
+                       "sp_relayout_inverse",
                        "chain_check", "chain_selftest_wait_timeout", "chain_umma_selftest",
                        "chain_last_cuda_error"):
                 getattr(lib, fn).restype = ci
@@ -143,6 +145,14 @@ def chain_fwd(A, B, C, f, mask, scale, O, LSE=None, stream=None):
     _ok(_load().chain_fwd(_ref(desc(A)), _ref(desc(B)), _ref(desc(C)), int(f), int(mask),
                           float(scale), _ref(desc(O)), _ref(desc(LSE)), _stream(stream)),
         "chain_fwd")
+
+
+def chain_fwd_sp(Q, K, V, p, head_group, mask, scale, O, LSE, stream=None):
+    """Attention of one head group read from and written to sequence shards
+    [p][n_loc][H][d]; see include/chain.h."""
+    _ok(_load().chain_fwd_sp(_ref(desc(Q)), _ref(desc(K)), _ref(desc(V)), int(p), int(head_group),
+                             int(mask), float(scale), _ref(desc(O)), _ref(desc(LSE)),
+                             _stream(stream)), "chain_fwd_sp")
 
 
 def chain_bwd_workspace_size(A, C) -> int:
@@ -218,6 +228,20 @@ def attention_fwd(q, k, v, causal: bool, scale: float | None = None, stream=None
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     chain_fwd(q, k, v, F_SOFTMAX, MASK_CAUSAL if causal else MASK_NONE, scale, o, lse, stream)
+    return o, lse
+
+
+def attention_fwd_sp(q, k, v, p: int, head_group: int, causal: bool, scale: float | None = None,
+                     o=None, stream=None):
+    """Shards q, k, v [p][n_loc][H][d] -> (O shards, LSE [H/p][p*n_loc]).  Only
+    the heads of `head_group` are written into `o` (a new zeroed tensor if
+    None)."""
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    P, n_loc, H, d = q.shape
+    if o is None:
+        o = torch.zeros_like(q)
+    lse = torch.empty(H // p, p * n_loc, dtype=torch.float32, device=q.device)
+    chain_fwd_sp(q, k, v, p, head_group, MASK_CAUSAL if causal else MASK_NONE, scale, o, lse, stream)
     return o, lse
 
 

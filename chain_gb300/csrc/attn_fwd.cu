@@ -61,9 +61,10 @@ struct FwdLayout {
 
 struct FwdParams {
   int BH, n, nqb2, nkb, causal;
+  int n_loc;  // positions per sequence shard (n when unsharded)
   float scale_log2;
   __nv_bfloat16 *O;
-  int64_t o_sbh, o_srow;
+  int64_t o_sbh, o_srow, o_sshard;
   float *LSE;
   int64_t lse_sbh;
   WaitCfg wc;
@@ -101,7 +102,7 @@ __device__ __forceinline__ int kv_tiles(const FwdParams &p, int qb, int t) {
   return last < p.nkb ? last : p.nkb;
 }
 
-template <int D>
+template <int D, bool SHARDED>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
@@ -169,13 +170,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       int k_issued = 0, v_issued = 0;
+      // 128-row box starting at sequence position `row`; over sequence
+      // shards: shard row / n_loc, row row % n_loc in it (a box never
+      // crosses a shard)
+      auto load = [&](uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int c0, int row) {
+        if constexpr (SHARDED) {
+          const int sh = row / p.n_loc;
+          tma_load_4d(dst, map, bar, c0, row - sh * p.n_loc, sh, bh);
+        } else {
+          tma_load_3d(dst, map, bar, c0, row, bh);
+        }
+      };
       mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
 #pragma unroll
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + L::OFF_Q + t * L::Q_BYTES + c * (BM * 128), &tmQ, q_full, c * 64,
-                      (2 * qb + t) * BM, bh);
+          load(smem + L::OFF_Q + t * L::Q_BYTES + c * (BM * 128), &tmQ, q_full, c * 64,
+               (2 * qb + t) * BM);
       for (int j = 0; j < nkv_b; ++j) {
         const int st = j % STAGES;
         if (j >= STAGES &&
@@ -184,8 +196,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive_expect_tx(&k_full[st], L::KV_BYTES);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + L::OFF_K + st * L::KV_BYTES + c * (BN * 128), &tmK, &k_full[st],
-                      c * 64, j * BN, bh);
+          load(smem + L::OFF_K + st * L::KV_BYTES + c * (BN * 128), &tmK, &k_full[st], c * 64,
+               j * BN);
         k_issued = j + 1;
         if (j >= STAGES &&
             !mbar_wait(&v_empty[st], ((j / STAGES) - 1) & 1, p.wc, abort_flag, SITE_FWD_PROD))
@@ -193,8 +205,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive_expect_tx(&v_full[st], L::KV_BYTES);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + L::OFF_V + st * L::KV_BYTES + c * (BN * 128), &tmV, &v_full[st],
-                      c * 64, j * BN, bh);
+          load(smem + L::OFF_V + st * L::KV_BYTES + c * (BN * 128), &tmV, &v_full[st], c * 64,
+               j * BN);
         v_issued = j + 1;
       }
       if (*abort_flag) {
@@ -402,7 +414,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok && mbar_wait(&pv_done[t], (nkv - 1) & 1, p.wc, abort_flag, SITE_FWD_EPI)) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      __nv_bfloat16 *orow = p.O + (int64_t)bh * p.o_sbh + (int64_t)q_idx * p.o_srow;
+      const int q_sh = SHARDED ? q_idx / p.n_loc : 0;
+      __nv_bfloat16 *orow = p.O + (int64_t)bh * p.o_sbh + (int64_t)q_sh * p.o_sshard +
+                            (int64_t)(q_idx - q_sh * p.n_loc) * p.o_srow;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -437,18 +451,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 template <int D>
 cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t st) {
   using L = FwdLayout<D>;
+  // Tensor maps {d, row, head} for one contiguous sequence; {d, row in
+  // shard, shard, head} over sequence shards.
   CUtensorMap mq, mk, mv;
-  const uint32_t box[3] = {64, 128, 1};
-  const uint64_t dims[3] = {(uint64_t)a.d, (uint64_t)a.n, (uint64_t)a.BH};
-  uint64_t sq[2] = {(uint64_t)a.q_srow * 2, (uint64_t)a.q_sbh * 2};
-  uint64_t sk[2] = {(uint64_t)a.k_srow * 2, (uint64_t)a.k_sbh * 2};
-  uint64_t sv[2] = {(uint64_t)a.v_srow * 2, (uint64_t)a.v_sbh * 2};
+  const bool sharded = a.n_loc != a.n;
+  const int rank = sharded ? 4 : 3;
+  const int nsh = a.n / a.n_loc;
+  const uint32_t box[4] = {64, 128, 1, 1};
+  uint64_t dims[4] = {(uint64_t)a.d, (uint64_t)a.n_loc, (uint64_t)nsh, (uint64_t)a.BH};
+  uint64_t sq[3] = {(uint64_t)a.q_srow * 2, (uint64_t)a.q_sshard * 2, (uint64_t)a.q_sbh * 2};
+  uint64_t sk[3] = {(uint64_t)a.k_srow * 2, (uint64_t)a.k_sshard * 2, (uint64_t)a.k_sbh * 2};
+  uint64_t sv[3] = {(uint64_t)a.v_srow * 2, (uint64_t)a.v_sshard * 2, (uint64_t)a.v_sbh * 2};
+  if (!sharded) {  // drop the shard dimension
+    dims[2] = dims[3];
+    sq[1] = sq[2];
+    sk[1] = sk[2];
+    sv[1] = sv[2];
+  }
   cudaError_t e;
-  if ((e = make_tmap(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.Q, dims, sq, box)) != cudaSuccess)
+  if ((e = make_tmap(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, a.Q, dims, sq, box)) != cudaSuccess)
     return e;
-  if ((e = make_tmap(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.K, dims, sk, box)) != cudaSuccess)
+  if ((e = make_tmap(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, a.K, dims, sk, box)) != cudaSuccess)
     return e;
-  if ((e = make_tmap(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.V, dims, sv, box)) != cudaSuccess)
+  if ((e = make_tmap(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, a.V, dims, sv, box)) != cudaSuccess)
     return e;
   FwdParams p;
   p.BH = a.BH;
@@ -460,10 +485,12 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t s
   p.O = static_cast<__nv_bfloat16 *>(a.O);
   p.o_sbh = a.o_sbh;
   p.o_srow = a.o_srow;
+  p.o_sshard = a.o_sshard;
+  p.n_loc = a.n_loc;
   p.LSE = a.LSE;
   p.lse_sbh = a.lse_sbh;
   p.wc = wc;
-  auto kern = attn_fwd_kernel<D>;
+  auto kern = sharded ? attn_fwd_kernel<D, true> : attn_fwd_kernel<D, false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(p.nqb2 * a.BH);

@@ -298,6 +298,8 @@ int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B, const chain_tens
     args.LSE = static_cast<float *>(LSE->ptr); args.lse_sbh = lse_sbh;
     args.BH = (int)a.outer; args.n = (int)a.rows; args.d = (int)a.cols;
     args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
+    args.n_loc = args.n;
+    args.q_sshard = args.k_sshard = args.v_sshard = args.o_sshard = 0;
     DevInfo *di = nullptr;
     if ((rc = device_ready(&di))) return rc;
     cudaError_t e;
@@ -414,6 +416,56 @@ static int relayout_common(const chain_tensor_t *seq, const chain_tensor_t *hm, 
                                             static_cast<cudaStream_t>(stream))
                           : launch_relayout(seq->ptr, hm->ptr, p, n_loc, H, row_bytes, g, 0,
                                             static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
+}
+
+// A [p][n_loc][H][d] sequence-shard tensor, d contiguous, strides in 16-byte
+// multiples, 16-byte aligned.
+static int shard_view(const chain_tensor_t *t, int64_t p, int64_t n_loc, int64_t H, int64_t d) {
+  if (!t || !t->ptr || t->ndim != 4) return CHAIN_ERR_ARG;
+  if (t->dtype != CHAIN_BF16) return CHAIN_ERR_DTYPE;
+  if (t->shape[0] != p || t->shape[1] != n_loc || t->shape[2] != H || t->shape[3] != d)
+    return CHAIN_ERR_ARG;
+  if (t->stride[3] != 1 || !aligned16(t->ptr)) return CHAIN_ERR_ARG;
+  for (int i = 0; i < 3; ++i)
+    if (t->stride[i] <= 0 || (t->stride[i] * 2) % 16) return CHAIN_ERR_ARG;
+  return CHAIN_OK;
+}
+
+int chain_fwd_sp(const chain_tensor_t *Q, const chain_tensor_t *K, const chain_tensor_t *V,
+                 int p, int head_group, int mask, float scale, chain_tensor_t *O,
+                 chain_tensor_t *LSE, void *stream) {
+  if (!Q || Q->ndim != 4) return CHAIN_ERR_ARG;
+  if (mask != CHAIN_MASK_NONE && mask != CHAIN_MASK_CAUSAL) return CHAIN_ERR_ARG;
+  if (p <= 0 || head_group < 0 || head_group >= p) return CHAIN_ERR_ARG;
+  const int64_t n_loc = Q->shape[1], H = Q->shape[2], d = Q->shape[3];
+  int rc;
+  if ((rc = shard_view(Q, p, n_loc, H, d)) || (rc = shard_view(K, p, n_loc, H, d)) ||
+      (rc = shard_view(V, p, n_loc, H, d)) || (rc = shard_view(O, p, n_loc, H, d)))
+    return rc;
+  if (n_loc <= 0 || H <= 0 || H % p || (d != 64 && d != 128)) return CHAIN_ERR_ARG;
+  if (!(scale > 0.0f) || !(scale < 1e30f)) return CHAIN_ERR_ARG;
+  const int64_t Hl = H / p, n = p * n_loc;
+  if (n > (1 << 30) || Hl > 65535 * 16) return CHAIN_ERR_ARG;
+  if (n_loc % 128) return CHAIN_ERR_UNSUPPORTED;  // a 128-row tile must not cross shards
+  int64_t lse_sbh = 0;
+  if ((rc = lse_view(LSE, Hl, n, &lse_sbh))) return rc;
+  const int64_t h0 = (int64_t)head_group * Hl;
+  AttnFwdArgs args;
+  args.Q = static_cast<const __nv_bfloat16 *>(Q->ptr) + h0 * Q->stride[2];
+  args.K = static_cast<const __nv_bfloat16 *>(K->ptr) + h0 * K->stride[2];
+  args.V = static_cast<const __nv_bfloat16 *>(V->ptr) + h0 * V->stride[2];
+  args.O = static_cast<__nv_bfloat16 *>(O->ptr) + h0 * O->stride[2];
+  args.q_sbh = Q->stride[2]; args.q_srow = Q->stride[1]; args.q_sshard = Q->stride[0];
+  args.k_sbh = K->stride[2]; args.k_srow = K->stride[1]; args.k_sshard = K->stride[0];
+  args.v_sbh = V->stride[2]; args.v_srow = V->stride[1]; args.v_sshard = V->stride[0];
+  args.o_sbh = O->stride[2]; args.o_srow = O->stride[1]; args.o_sshard = O->stride[0];
+  args.LSE = static_cast<float *>(LSE->ptr); args.lse_sbh = lse_sbh;
+  args.BH = (int)Hl; args.n = (int)n; args.d = (int)d; args.n_loc = (int)n_loc;
+  args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
+  DevInfo *di = nullptr;
+  if ((rc = device_ready(&di))) return rc;
+  cudaError_t e = launch_attn_fwd_bf16(args, wait_cfg(di), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
 }
 

@@ -24,6 +24,10 @@ struct AttnFwdArgs {
   int64_t lse_sbh;
   int BH, n, d, causal;
   float scale;
+  // Sequence split into n / n_loc shards: position s*n_loc + t lives at
+  // s*x_sshard + t*x_srow (elements).  n_loc = n for one contiguous run.
+  int n_loc;
+  int64_t q_sshard, k_sshard, v_sshard, o_sshard;
 };
 
 cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t st);

@@ -135,6 +135,15 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *map, uint64_t
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void *dst, const void *map, uint64_t *bar, int c0,
+                                            int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *map, uint64_t *bar, int c0,
                                             int c1) {
   asm volatile(

@@ -167,6 +167,36 @@ int chain_bwd_noalloc(const chain_tensor_t *dO, const chain_tensor_t *A,
                       chain_tensor_t *dB, chain_tensor_t *dC, void *stream);
 
 /*
+ * chain_fwd_sp -- softmax attention read from, and written back to, the
+ * Ulysses sequence-shard layout: the all-to-all relayout of Q, K and V, the
+ * attention of one head group over the whole sequence, and the inverse
+ * relayout of O, in one kernel ("Ulysses Sequence Parallelism", "Contexte
+ * Technique" and "Analyse et Implications"; the unit is the O = f(A B) C of
+ * "Memory-efficient tensor parallelism", FITEE 10.1631/FITEE.2400602).  The
+ * head-major copies never exist in memory: the tensor-core loads read 128-row
+ * boxes straight out of the shards.
+ *   Q, K, V, O  [p][n_loc][H][d] bf16: shard s holds positions
+ *               [s*n_loc, (s+1)*n_loc); d = 64 or 128, contiguous; other
+ *               strides multiples of 16 bytes; 16-byte aligned.  O may have
+ *               its own strides.
+ *   head_group  g in [0, p): the call attends heads [g*H/p, (g+1)*H/p) over
+ *               all n = p*n_loc positions and writes exactly those heads of
+ *               O; the other heads of O are left untouched.
+ *   mask, scale as for chain_fwd with f = CHAIN_F_SOFTMAX.
+ *   LSE         [H/p][n] fp32, natural log, head-major (h relative to the
+ *               group).
+ * Same results, bit for bit, as sp_relayout of Q, K and V, then chain_fwd,
+ * then sp_relayout_inverse of O.  Returns CHAIN_ERR_UNSUPPORTED unless n_loc
+ * is a multiple of 128 (a tile must not straddle two shards), CHAIN_ERR_ARG
+ * for a shape, stride or alignment violation, CHAIN_ERR_DTYPE unless bf16.
+ * Asynchronous on `stream`.
+ */
+int chain_fwd_sp(const chain_tensor_t *Q, const chain_tensor_t *K,
+                 const chain_tensor_t *V, int p, int head_group, int mask,
+                 float scale, chain_tensor_t *O, chain_tensor_t *LSE,
+                 void *stream);
+
+/*
  * sp_relayout -- Ulysses sequence shards -> head-major for one head group
  * ("Ulysses Sequence Parallelism", "Contexte Technique": every position of
  * the sequence, a subset of the heads).
