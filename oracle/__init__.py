@@ -57,10 +57,13 @@ def _load():
                                                ci, i64, i64, i64, i64, i64, i64, vp, vp, vp, vp]
             lib.oracle_chain_fwd.argtypes = [ci, vp, vp, vp, i64, i64, i64, i64, ci, dbl,
                                              i64, vp, vp]
+            lib.oracle_chain_bwd.argtypes = [ci, vp, vp, vp, vp, i64, i64, i64, i64, ci, i64, vp,
+                                             i64, vp, vp, vp, vp]
             lib.oracle_relayout.argtypes = [vp, i64, i64, i64, i64, i64, i64, vp]
             lib.oracle_relayout_inverse.argtypes = [vp, i64, i64, i64, i64, i64, i64, vp]
             for fn in ("oracle_softmax_fwd", "oracle_softmax_fwd_blocked", "oracle_softmax_bwd",
-                       "oracle_chain_fwd", "oracle_relayout", "oracle_relayout_inverse"):
+                       "oracle_chain_fwd", "oracle_chain_bwd", "oracle_relayout",
+                       "oracle_relayout_inverse"):
                 getattr(lib, fn).restype = ci
             _lib = lib
     return _lib
@@ -196,6 +199,34 @@ def chain_fwd(A, B, C, f: int, scale: float = 1.0, rows=None):
     if rc != 0:
         raise RuntimeError(f"oracle_chain_fwd failed ({rc})")
     return O
+
+
+def chain_bwd(A, B, C, dO, f: int, rows=None, hidden=None):
+    """Backward of O = f(A B) C (f identity or gelu_tanh), the intermediate
+    recomputed.  A [M,K], B [K,N], C [N,P], dO [M,P].
+
+    Returns (dA_rows [R,K], dB_cols [RH,K], dC_rows [RH,P]): rows `rows` of
+    dA (None = all) and, for hidden units `hidden` (None = all), column h of
+    dB (stored as a row) and row h of dC."""
+    a, b, c, g = _raw(A), _raw(B), _raw(C), _raw(dO)
+    dt = _same(a, b, c, g)
+    M, K = a[0].shape
+    K2, N = b[0].shape
+    N2, P = c[0].shape
+    if K2 != K or N2 != N or g[0].shape != (M, P):
+        raise ValueError("oracle.chain_bwd: shapes differ")
+    ra = (np.arange(M, dtype=np.int64) if rows is None
+          else np.ascontiguousarray(np.asarray(rows, dtype=np.int64)))
+    rh = (np.arange(N, dtype=np.int64) if hidden is None
+          else np.ascontiguousarray(np.asarray(hidden, dtype=np.int64)))
+    dA = np.empty((ra.shape[0], K), np.float64)
+    dB = np.empty((rh.shape[0], K), np.float64)
+    dC = np.empty((rh.shape[0], P), np.float64)
+    rc = _load().oracle_chain_bwd(dt, _p(a[0]), _p(b[0]), _p(c[0]), _p(g[0]), M, K, N, P, int(f),
+                                  ra.shape[0], _p(ra), rh.shape[0], _p(rh), _p(dA), _p(dB), _p(dC))
+    if rc != 0:
+        raise RuntimeError(f"oracle_chain_bwd failed ({rc})")
+    return dA, dB, dC
 
 
 def _bytes_view(x):

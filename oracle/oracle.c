@@ -366,6 +366,99 @@ int oracle_chain_fwd(int dtype, const void *A, const void *B, const void *C,
   return bad ? -3 : 0;
 }
 
+/* derivative of the tanh form of GeLU: with u = k (t + 0.044715 t^3),
+ * k = sqrt(2/pi):  0.5 (1 + tanh u) + 0.5 t (1 - tanh^2 u) k (1 + 3*0.044715 t^2) */
+static double gelu_tanh_grad(double t) {
+  const double k = sqrt(2.0 / M_PI);
+  const double th = tanh(k * (t + 0.044715 * t * t * t));
+  return 0.5 * (1.0 + th) + 0.5 * t * (1.0 - th * th) * k * (1.0 + 3.0 * 0.044715 * t * t);
+}
+
+/* ------------------------------------------------------------------------
+ * Backward of the chain O = f(A B) C for f = identity or gelu_tanh, the
+ * intermediate recomputed from A and B instead of stored (AutoSP, section
+ * 2.B).  Given dO [M][P], by the chain rule:
+ *   T = A B,  H = f(T),  dH = dO C^T,  dT = dH * f'(T)   (elementwise)
+ *   dC = H^T dO,   dA = dT B^T,   dB = A^T dT.
+ * Outputs for requested rows ra of dA:            dA_out [RA][K]
+ * and requested hidden units rh: row h of dC,      dC_out [RH][P]
+ *                                column h of dB,   dB_out [RH][K]
+ * Everything in double; T, H, dH, dT are never rounded.
+ * ---------------------------------------------------------------------- */
+int oracle_chain_bwd(int dtype, const void *A, const void *B, const void *C, const void *dO,
+                     int64_t M, int64_t K, int64_t N, int64_t P, int f, int64_t RA,
+                     const int64_t *ra, int64_t RH, const int64_t *rh, double *dA_out,
+                     double *dB_out, double *dC_out) {
+  if (M <= 0 || K <= 0 || N <= 0 || P <= 0) return -1;
+  if (f != ORACLE_F_IDENTITY && f != ORACLE_F_GELU_TANH) return -1;
+  for (int64_t r = 0; r < RA; ++r)
+    if (ra[r] < 0 || ra[r] >= M) return -2;
+  for (int64_t r = 0; r < RH; ++r)
+    if (rh[r] < 0 || rh[r] >= N) return -2;
+  int bad = 0;
+  /* rows of dA: one full row of T, dH and dT per requested row */
+#pragma omp parallel
+  {
+    double *dT = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!dT) {
+#pragma omp atomic write
+      bad = 1;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t r = 0; r < RA; ++r) {
+      if (!dT) continue;
+      const int64_t a = ra[r];
+      for (int64_t c = 0; c < N; ++c) {
+        double t = 0.0, dh = 0.0;
+        for (int64_t k = 0; k < K; ++k) t += elem(A, dtype, a * K + k) * elem(B, dtype, k * N + c);
+        for (int64_t e = 0; e < P; ++e) dh += elem(dO, dtype, a * P + e) * elem(C, dtype, c * P + e);
+        dT[c] = dh * (f == ORACLE_F_GELU_TANH ? gelu_tanh_grad(t) : 1.0);
+      }
+      for (int64_t k = 0; k < K; ++k) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < N; ++c) acc += dT[c] * elem(B, dtype, k * N + c);
+        dA_out[r * K + k] = acc;
+      }
+    }
+    free(dT);
+  }
+  /* hidden units: the full column h of T, H, dH and dT over all M rows */
+#pragma omp parallel
+  {
+    double *Hc = (double *)malloc(sizeof(double) * (size_t)M);
+    double *dTc = (double *)malloc(sizeof(double) * (size_t)M);
+    if (!Hc || !dTc) {
+#pragma omp atomic write
+      bad = 1;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t r = 0; r < RH; ++r) {
+      if (!Hc || !dTc) continue;
+      const int64_t h = rh[r];
+      for (int64_t m = 0; m < M; ++m) {
+        double t = 0.0, dh = 0.0;
+        for (int64_t k = 0; k < K; ++k) t += elem(A, dtype, m * K + k) * elem(B, dtype, k * N + h);
+        for (int64_t e = 0; e < P; ++e) dh += elem(dO, dtype, m * P + e) * elem(C, dtype, h * P + e);
+        Hc[m] = f == ORACLE_F_GELU_TANH ? gelu_tanh(t) : t;
+        dTc[m] = dh * (f == ORACLE_F_GELU_TANH ? gelu_tanh_grad(t) : 1.0);
+      }
+      for (int64_t e = 0; e < P; ++e) {
+        double acc = 0.0;
+        for (int64_t m = 0; m < M; ++m) acc += Hc[m] * elem(dO, dtype, m * P + e);
+        dC_out[r * P + e] = acc;
+      }
+      for (int64_t k = 0; k < K; ++k) {
+        double acc = 0.0;
+        for (int64_t m = 0; m < M; ++m) acc += elem(A, dtype, m * K + k) * dTc[m];
+        dB_out[r * K + k] = acc;
+      }
+    }
+    free(Hc);
+    free(dTc);
+  }
+  return bad ? -3 : 0;
+}
+
 /* ------------------------------------------------------------------------
  * Ulysses sequence-shard -> head-major redistribution ("Contexte
  * Technique": after the exchange each device holds every sequence position

@@ -277,6 +277,77 @@ def test_chain_sampled_rows(orc):
     assert np.array_equal(Os, O[rows])
 
 
+# ------------------------------------------------------------ chain backward
+def _chain_loss(orc, A, B, C, G, f):
+    return float((orc.chain_fwd(A, B, C, f) * G).sum())
+
+
+@pytest.mark.parametrize("f", ["gelu", "identity"])
+def test_chain_bwd_finite_differences(orc, f):
+    # Central differences of L = sum(O * G) through the oracle's forward.
+    fc = orc.F_GELU_TANH if f == "gelu" else orc.F_IDENTITY
+    rng = np.random.default_rng(91)
+    A, B, C, G = (rng.standard_normal(sh) for sh in ((3, 4), (4, 5), (5, 2), (3, 2)))
+    dA, dBc, dC = orc.chain_bwd(A, B, C, G, fc)
+    h = 1e-6
+    for name, X, grad in (("A", A, dA), ("B", B, dBc.T), ("C", C, dC)):
+        num = np.zeros_like(X)
+        for idx in np.ndindex(*X.shape):
+            xp, xm = X.copy(), X.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = {"A": A, "B": B, "C": C}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = xp, xm
+            num[idx] = (_chain_loss(orc, args_p["A"], args_p["B"], args_p["C"], G, fc)
+                        - _chain_loss(orc, args_m["A"], args_m["B"], args_m["C"], G, fc)) / (2 * h)
+        assert rel(grad, num) < 1e-7, (f, name)
+
+
+def test_chain_bwd_identity_closed_form(orc):
+    # f = identity: dA = G C^T B^T, dB = A^T G C^T, dC = (A B)^T G.
+    rng = np.random.default_rng(92)
+    A, B, C, G = (rng.standard_normal(sh) for sh in ((19, 11), (11, 23), (23, 7), (19, 7)))
+    dA, dBc, dC = orc.chain_bwd(A, B, C, G, orc.F_IDENTITY)
+    assert rel(dA, G @ C.T @ B.T) < 1e-12
+    assert rel(dBc.T, A.T @ G @ C.T) < 1e-12
+    assert rel(dC, (A @ B).T @ G) < 1e-12
+
+
+def test_chain_bwd_vs_autograd(orc):
+    # fp64 autograd of the library's tanh GeLU, an independent derivative.
+    rng = np.random.default_rng(93)
+    A, B, C, G = (torch.from_numpy(rng.standard_normal(sh) * sc)
+                  for sh, sc in (((17, 9), 1.0), ((9, 31), 0.7), ((31, 5), 0.4), ((17, 5), 1.0)))
+    A.requires_grad_(True)
+    B.requires_grad_(True)
+    C.requires_grad_(True)
+    O = torch.nn.functional.gelu(A @ B, approximate="tanh") @ C
+    (O * G).sum().backward()
+    dA, dBc, dC = orc.chain_bwd(A.detach(), B.detach(), C.detach(), G, orc.F_GELU_TANH)
+    assert rel(dA, A.grad.numpy()) < 1e-12
+    assert rel(dBc.T, B.grad.numpy()) < 1e-12
+    assert rel(dC, C.grad.numpy()) < 1e-12
+
+
+def test_gelu_grad_symmetry(orc):
+    # gelu(x) - gelu(-x) = x, so gelu'(x) + gelu'(-x) = 1; gelu'(0) = 1/2.
+    one = np.ones((1, 1))
+    for t in (0.0, 0.3, -1.7, 2.5, 6.0):
+        g = lambda x: orc.chain_bwd(np.array([[x]]), one, one, one, orc.F_GELU_TANH)[0][0, 0]
+        assert abs(g(t) + g(-t) - 1.0) < 1e-14, t
+    assert abs(orc.chain_bwd(np.zeros((1, 1)), one, one, one, orc.F_GELU_TANH)[0][0, 0] - 0.5) < 1e-15
+
+
+def test_chain_bwd_sampled_match_full(orc):
+    A, B, C = cs.mlp_inputs(40, 16, 24, 8, seed=94)
+    G = cs.normal((40, 8), seed=95)
+    dA, dB, dC = orc.chain_bwd(A, B, C, G, orc.F_GELU_TANH)
+    rows, hid = [0, 7, 39], [1, 23, 10]
+    sA, sB, sC = orc.chain_bwd(A, B, C, G, orc.F_GELU_TANH, rows=rows, hidden=hid)
+    assert np.array_equal(sA, dA[rows]) and np.array_equal(sB, dB[hid]) and np.array_equal(sC, dC[hid])
+
+
 # ------------------------------------------------------------------ relayout
 @pytest.mark.parametrize("p,n_loc,H,d,g", [(4, 5, 8, 3, 0), (4, 5, 8, 3, 3), (2, 7, 6, 4, 1)])
 def test_relayout_vs_transpose(orc, p, n_loc, H, d, g):
