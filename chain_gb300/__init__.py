@@ -70,6 +70,8 @@ def _load():
             lib.chain_bwd_noalloc.argtypes = [P, P, P, P, P, P, ci, ci, fl, P, P, P, vp]
             lib.chain_bwd_workspace_size.argtypes = [P, P]
             lib.chain_bwd_workspace_size.restype = ctypes.c_size_t
+            lib.chain_bwd_workspace_size_f.argtypes = [P, P, ci]
+            lib.chain_bwd_workspace_size_f.restype = ctypes.c_size_t
             lib.chain_fwd_sp.argtypes = [P, P, P, ci, ci, ci, fl, P, P, vp]
             lib.sp_relayout.argtypes = [P, ci, ci, P, vp]
             lib.sp_relayout_inverse.argtypes = [P, ci, ci, P, vp]
@@ -157,6 +159,10 @@ def chain_fwd_sp(Q, K, V, p, head_group, mask, scale, O, LSE, stream=None):
 
 def chain_bwd_workspace_size(A, C) -> int:
     return int(_load().chain_bwd_workspace_size(_ref(desc(A)), _ref(desc(C))))
+
+
+def chain_bwd_workspace_size_f(A, C, f) -> int:
+    return int(_load().chain_bwd_workspace_size_f(_ref(desc(A)), _ref(desc(C)), int(f)))
 
 
 def chain_bwd(dO, A, B, C, O, LSE, f, mask, scale, dA, dB, dC, workspace, stream=None):
@@ -263,6 +269,17 @@ def mlp_chain_fwd(x, w1, w2, gelu: bool = True, stream=None):
     o = torch.empty(x.shape[0], w2.shape[1], dtype=x.dtype, device=x.device)
     chain_fwd(x, w1, w2, F_GELU_TANH if gelu else F_IDENTITY, MASK_NONE, 1.0, o, None, stream)
     return o
+
+
+def mlp_chain_bwd(do, x, w1, w2, gelu: bool = True, workspace=None, stream=None):
+    """Returns (dX, dW1, dW2) of O = gelu_tanh(x w1) w2 (or identity)."""
+    f = F_GELU_TANH if gelu else F_IDENTITY
+    if workspace is None:
+        workspace = torch.empty(chain_bwd_workspace_size_f(x, w2, f), dtype=torch.uint8,
+                                device=x.device)
+    dx, dw1, dw2 = torch.empty_like(x), torch.empty_like(w1), torch.empty_like(w2)
+    chain_bwd(do, x, w1, w2, None, None, f, MASK_NONE, 1.0, dx, dw1, dw2, workspace, stream)
+    return dx, dw1, dw2
 
 
 def relayout(shards, p: int, head_group: int, stream=None):

@@ -336,12 +336,68 @@ int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B, const chain_tens
   return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
 }
 
+static size_t mlp_ws_bytes(const View &a, const View &c) {
+  // H and dT, [M][N] bf16 each (M = rows of X, N = rows of W2)
+  const size_t b = (size_t)a.rows * (size_t)c.rows * 2 * 2;
+  return (b + 255) & ~size_t(255);
+}
+
 size_t chain_bwd_workspace_size(const chain_tensor_t *A, const chain_tensor_t *C) {
   View a, c;
   if (view_of(A, 2, &a) || view_of(C, 2, &c)) return 0;
-  if (!same_shape(a, c)) return 0;
+  if (!same_shape(a, c)) {
+    // different shapes: the MLP chain (A = X [M][K], C = W2 [N][P])
+    if (A->ndim != 2 || C->ndim != 2) return 0;
+    return mlp_ws_bytes(a, c);
+  }
   const size_t dvec = (size_t)a.outer * a.rows * sizeof(float);
   return (dvec + 255) & ~size_t(255);
+}
+
+size_t chain_bwd_workspace_size_f(const chain_tensor_t *A, const chain_tensor_t *C, int f) {
+  if (f == CHAIN_F_SOFTMAX) {
+    View a, c;
+    if (view_of(A, 2, &a) || view_of(C, 2, &c) || !same_shape(a, c)) return 0;
+    return ((size_t)a.outer * a.rows * sizeof(float) + 255) & ~size_t(255);
+  }
+  if (f != CHAIN_F_IDENTITY && f != CHAIN_F_GELU_TANH) return 0;
+  View a, c;
+  if (!A || !C || A->ndim != 2 || C->ndim != 2 || view_of(A, 2, &a) || view_of(C, 2, &c)) return 0;
+  return mlp_ws_bytes(a, c);
+}
+
+// Backward of the MLP chain O = f(X W1) W2: dense row-major 2-D bf16.
+static int mlp_bwd(const chain_tensor_t *dO, const chain_tensor_t *A, const chain_tensor_t *B,
+                   const chain_tensor_t *C, int f, int mask, chain_tensor_t *dA,
+                   chain_tensor_t *dB, chain_tensor_t *dC, void *workspace, size_t ws_bytes,
+                   void *stream) {
+  if (mask != CHAIN_MASK_NONE) return CHAIN_ERR_ARG;
+  const chain_tensor_t *ts[7] = {dO, A, B, C, dA, dB, dC};
+  View v[7];
+  for (int i = 0; i < 7; ++i) {
+    if (!ts[i] || ts[i]->ndim != 2) return CHAIN_ERR_ARG;
+    int rc = view_of(ts[i], 2, &v[i]);
+    if (rc) return rc;
+    if (v[i].dtype != CHAIN_BF16) return CHAIN_ERR_DTYPE;
+    if (v[i].s_row != v[i].cols || !aligned16(v[i].ptr)) return CHAIN_ERR_ARG;
+  }
+  const View &g = v[0], &x = v[1], &w1 = v[2], &w2 = v[3], &dx = v[4], &dw1 = v[5], &dw2 = v[6];
+  const int64_t M = x.rows, K = x.cols, N = w1.cols, P = w2.cols;
+  if (w1.rows != K || w2.rows != N || g.rows != M || g.cols != P) return CHAIN_ERR_ARG;
+  if (!same_shape(dx, x) || !same_shape(dw1, w1) || !same_shape(dw2, w2)) return CHAIN_ERR_ARG;
+  if (M <= 0 || K <= 0 || N <= 0 || P <= 0 || M * N >= (int64_t(1) << 36)) return CHAIN_ERR_ARG;
+  if (M % 128 || K % 256 || N % 256 || P % 256) return CHAIN_ERR_UNSUPPORTED;
+  if (!workspace || ws_bytes < mlp_ws_bytes(x, w2) || !aligned16(workspace)) return CHAIN_ERR_ARG;
+  MlpBwdArgs m;
+  m.X = x.ptr; m.W1 = w1.ptr; m.W2 = w2.ptr; m.dO = g.ptr;
+  m.dX = dx.ptr; m.dW1 = dw1.ptr; m.dW2 = dw2.ptr; m.workspace = workspace;
+  m.M = (int)M; m.K = (int)K; m.N = (int)N; m.P = (int)P; m.gelu = f == CHAIN_F_GELU_TANH;
+  DevInfo *di = nullptr;
+  int rc = device_ready(&di);
+  if (rc) return rc;
+  cudaError_t e = launch_mlp_bwd(m, wait_cfg(di), static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return CHAIN_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
 }
 
 int chain_bwd(const chain_tensor_t *dO, const chain_tensor_t *A, const chain_tensor_t *B,
@@ -349,7 +405,8 @@ int chain_bwd(const chain_tensor_t *dO, const chain_tensor_t *A, const chain_ten
               int mask, float scale, chain_tensor_t *dA, chain_tensor_t *dB, chain_tensor_t *dC,
               void *workspace, size_t ws_bytes, void *stream) {
   if (f != CHAIN_F_SOFTMAX) {
-    if (f == CHAIN_F_IDENTITY || f == CHAIN_F_GELU_TANH) return CHAIN_ERR_UNSUPPORTED;
+    if (f == CHAIN_F_IDENTITY || f == CHAIN_F_GELU_TANH)
+      return mlp_bwd(dO, A, B, C, f, mask, dA, dB, dC, workspace, ws_bytes, stream);
     return CHAIN_ERR_ARG;
   }
   if (mask != CHAIN_MASK_NONE && mask != CHAIN_MASK_CAUSAL) return CHAIN_ERR_ARG;

@@ -43,6 +43,14 @@ struct AttnBwdArgs {
 };
 cudaError_t launch_attn_bwd(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t st);
 
+struct MlpBwdArgs {
+  const void *X, *W1, *W2, *dO;  // [M][K], [K][N], [N][P], [M][P] bf16 row-major
+  void *dX, *dW1, *dW2;          // [M][K], [K][N], [N][P] bf16
+  void *workspace;               // H and dT, [M][N] bf16 each
+  int M, K, N, P, gelu;
+};
+cudaError_t launch_mlp_bwd(const MlpBwdArgs &a, const WaitCfg &wc, cudaStream_t st);
+
 struct MlpArgs {
   const void *X, *W1, *W2;  // [M][K], [K][N], [N][P] bf16 row-major
   void *O;                  // [M][P] bf16

@@ -107,10 +107,19 @@ int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B,
 
 /*
  * chain_bwd_workspace_size -- bytes of device workspace chain_bwd needs for
- * these shapes: the fp32 [BH][n] row term D, rounded up to 256 bytes.
- * Returns 0 for invalid descriptors.
+ * these shapes, rounded up to 256 bytes.  A and C of one shape mean the
+ * softmax chain: the fp32 [BH][n] row term D.  2-D A and C of different
+ * shapes mean the MLP chain (A = X [M][K], C = W2 [N][P]): H and dT, [M][N]
+ * bf16 each.  Returns 0 for invalid descriptors.
  */
 size_t chain_bwd_workspace_size(const chain_tensor_t *A, const chain_tensor_t *C);
+
+/*
+ * chain_bwd_workspace_size_f -- the same, with the chain named by f, for the
+ * MLP shapes chain_bwd_workspace_size cannot tell apart (X and W2 of one
+ * shape).  Returns 0 for invalid descriptors or f.
+ */
+size_t chain_bwd_workspace_size_f(const chain_tensor_t *A, const chain_tensor_t *C, int f);
 
 /*
  * chain_bwd -- gradients of the softmax chain (attention backward).
@@ -124,6 +133,19 @@ size_t chain_bwd_workspace_size(const chain_tensor_t *A, const chain_tensor_t *C
  *   accumulating on chip: no atomics, results are deterministic.
  *   workspace: device buffer of at least chain_bwd_workspace_size() bytes,
  *   16-byte aligned, contents ignored on entry.
+ *
+ * f = CHAIN_F_GELU_TANH or CHAIN_F_IDENTITY: gradients of the MLP chain
+ *   O = f(X W1) W2 ("Memory-efficient tensor parallelism", abstract), the
+ *   intermediate recomputed from X and W1 instead of kept from the forward
+ *   (AutoSP, section 2.B):
+ *     T = X W1, H = f(T), dH = dO W2^T, dT = dH * f'(T),
+ *     dW2 = H^T dO,  dX = dT W1^T,  dW1 = X^T dT.
+ *   dO [M][P], A = X [M][K], B = W1 [K][N], C = W2 [N][P] bf16, dense
+ *   row-major; O, LSE and scale are ignored (may be NULL / any); mask must be
+ *   CHAIN_MASK_NONE.  Outputs dA = dX [M][K], dB = dW1 [K][N], dC = dW2
+ *   [N][P] bf16.  H and dT go through the workspace as bf16 (fp32
+ *   accumulation everywhere else).  CHAIN_ERR_UNSUPPORTED unless M % 128 ==
+ *   0 and K, N, P are multiples of 256.
  */
 int chain_bwd(const chain_tensor_t *dO, const chain_tensor_t *A,
               const chain_tensor_t *B, const chain_tensor_t *C,
