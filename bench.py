@@ -469,6 +469,50 @@ def measure_sp_fused(hp, reps=5):
         "timing": f"median of {reps} after 2 warm-ups; inputs larger than L2"}}
 
 
+def measure_mlp_bwd(hp, reps=10):
+    """Backward of the GeLU MLP workload (intermediate recomputed): the
+    activation kernel and the batched product kernel, timed at their
+    boundaries.  Measured beside the step, not part of its value."""
+    torch, cg, m = hp.torch, hp.cg, hp.m
+    M, K, N, P = m["M"], m["K"], m["N"], m["P"]
+    gen = torch.Generator(device=hp.dev).manual_seed(5)
+    do = torch.randn(M, P, device=hp.dev, generator=gen).to(torch.bfloat16)
+    dx, dw1, dw2 = torch.empty_like(hp.x), torch.empty_like(hp.w1), torch.empty_like(hp.w2)
+    ws = torch.empty(cg.chain_bwd_workspace_size_f(hp.x, hp.w2, cg.F_GELU_TANH), dtype=torch.uint8,
+                     device=hp.dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=hp.dev)
+
+    def run(evs=None):
+        if evs is not None:
+            cg.set_timing_events(*evs)
+        cg.chain_bwd(do, hp.x, hp.w1, hp.w2, None, None, cg.F_GELU_TANH, cg.MASK_NONE, 1.0,
+                     dx, dw1, dw2, ws)
+        if evs is not None:
+            cg.set_timing_events()
+
+    for _ in range(3):
+        run()
+    tot, k1, k2 = [], [], []
+    for _ in range(reps):
+        flush.zero_()  # L2 flushed between iterations (the inputs fit in L2)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        run(evs)
+        torch.cuda.synchronize()
+        k1.append(evs[0].elapsed_time(evs[1]))
+        k2.append(evs[1].elapsed_time(evs[2]))
+        tot.append(evs[0].elapsed_time(evs[2]))
+    rc, site = cg.chain_check()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} site {site:#x} in the MLP backward measurement")
+    med = lambda v: sorted(v)[len(v) // 2]
+    fl = 4.0 * M * N * (P + K)  # dH, dW2, dX, dW1; the recomputed X W1 is not counted
+    ms = med(tot)
+    return {"gelu_mlp_bwd_4096x1024x4096x1024": {
+        "ms": round(ms, 4), "TFLOPs": round(fl / (ms * 1e-3) / 1e12, 1),
+        "act_kernel_ms": round(med(k1), 4), "gemm_kernel_ms": round(med(k2), 4),
+        "flops": fl, "timing": f"median of {reps}, L2 flushed between iterations"}}
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -650,9 +694,12 @@ def main():
         del hps
 
     # ---- NEXT rows, measured beside the step (not part of its value)
-    nxt = None
+    nxt = {}
     if hp.shards[0].numel() and (args.only is None or "sp" in args.only):
-        nxt = measure_sp_fused(hp)
+        nxt.update(measure_sp_fused(hp))
+    if hp.mlp_ok:
+        nxt.update(measure_mlp_bwd(hp))
+    nxt = nxt or None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
