@@ -7,7 +7,10 @@
 // second product; it is never written to global memory (the activation
 // the AutoSP write-up, section 2.B, recomputes instead of storing).
 //
-// One CTA per (128-row block of X, 256-column block of O).  For each
+// Two kernels.  The default (mlp_cluster_kernel, P/256 = 2..4) shares the
+// intermediate across a cluster so X W1 is formed once per row block; it is
+// described where it is defined.  The other, used for the remaining shapes:
+// one CTA per (128-row block of X, 256-column block of O).  For each
 // 128-wide hidden chunk c:
 //   GEMM1  T_c = X_blk W1[:, c]           (tcgen05, fp32 in tensor memory)
 //   f      H_c = f(T_c) in fp32 registers, split into H_hi = bf16(H_c) and
@@ -342,6 +345,322 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
+
+// ------------------------------------------------- cluster variant (default)
+// One cluster of CS = P/256 CTAs (2 to 4) per 128-row block; CTA q of the
+// cluster owns output columns [256q, 256q+256).  The hidden dimension runs in
+// 64-wide chunks c.  Chunk c is computed (GEMM1, f, hi/lo split) once, by CTA
+// k = c % CS, into its slot k; CTA k then pushes the 32 KB H_hi/H_lo tile
+// into slot k of every other CTA with bulk copies.  Every CTA runs GEMM2 over
+// all chunks.  X W1 is formed once per row block instead of once per output
+// block.
+//
+// Slot k is written only by CTA k:
+//   h_full[k]   in every CTA: the chunk in slot k is present (remote: the
+//               owner's copy completes the bytes the local MMA warp expects;
+//               own: the epilogue arrives after writing it)
+//   h_empty[k]  used in CTA k only: one multicast arrival from every CTA's
+//               GEMM2 of the chunk in slot k; CTA k waits for it (phase by
+//               phase) before overwriting the slot
+// A CTA leaves after its own GEMM2s, its last h_empty phase and its outgoing
+// copies have completed: then no peer can still write into its shared memory.
+constexpr int HC2 = 64;
+constexpr int MAX_CS = 4;
+
+struct ClusterLayout {
+  static constexpr int NST = 3;
+  static constexpr uint32_t OFF_RING = 0;
+  static constexpr uint32_t OFF_SLOT = OFF_RING + NST * STAGE_BYTES;  // [MAX_CS] x (hi 16 KB, lo 16 KB)
+  static constexpr uint32_t SLOT_BYTES = 32768;
+  static constexpr uint32_t OFF_BAR = OFF_SLOT + MAX_CS * SLOT_BYTES;
+  // full[3], empty[3], t_full[2], t_free[2], h_full[4], h_empty[4], o_done, mma_drain
+  static constexpr uint32_t NBAR = 2 * NST + 4 + 2 * MAX_CS + 2;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
+};
+
+struct ClusterParams {
+  int M, K, N, P, gelu, CS;
+  __nv_bfloat16 *O;
+  WaitCfg wc;
+};
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    mlp_cluster_kernel(const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmW1,
+                       const __grid_constant__ CUtensorMap tmW2, const ClusterParams p) {
+  using L = ClusterLayout;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+  uint64_t *full = bars;                  // [NST]
+  uint64_t *empty = bars + L::NST;        // [NST]
+  uint64_t *t_full = bars + 2 * L::NST;   // [2]
+  uint64_t *t_free = t_full + 2;          // [2], 128 arrivals
+  uint64_t *h_full = t_free + 2;          // [MAX_CS]
+  uint64_t *h_empty = h_full + MAX_CS;    // [MAX_CS], CS arrivals
+  uint64_t *o_done = h_empty + MAX_CS;
+  uint64_t *mma_drain = o_done + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int CS = p.CS;
+  const int q = (int)cluster_ctarank();
+  const int rb = blockIdx.x / CS;
+  const int NC = p.N / HC2;   // hidden chunks
+  const int NKT = p.K / KT;   // GEMM1 K-tiles per chunk
+  const int n_own = (NC - q + CS - 1) / CS;  // chunks q, q+CS, ...
+  const int n_pair = (n_own + 1) / 2;        // GEMM1 runs on pairs (q+2jCS, q+(2j+1)CS)
+  const uint32_t slot0 = smem_u32(smem + L::OFF_SLOT);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < L::NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&t_full[b], 1);
+      mbar_init(&t_free[b], 128);
+    }
+    for (int k = 0; k < MAX_CS; ++k) {
+      mbar_init(&h_full[k], 1);
+      mbar_init(&h_empty[k], (uint32_t)CS);
+    }
+    mbar_init(o_done, 1);
+    mbar_init(mma_drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW1);
+    tma_prefetch_desc(&tmW2);
+  }
+  tc_fence_before();
+  // every CTA's barriers exist before any peer signals them
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // T buffers [0,128), [128,256) (a pair each); O [256,512)
+
+  if (warp == 4) {
+    // -------------------------------------------------------- producer
+    // Consumption order of the MMA warp: GEMM1 of pair 0; then for each
+    // chunk c: GEMM1 of the next pair when c opens a pair, then the W2 tile
+    // of c.  A pair's W1 tile is two 64-column boxes (chunks c0 and c0+CS);
+    // a missing second chunk reads as zeros (past N).
+    if (lane == 0) {
+      int st = 0;
+      bool ok = true;
+      auto stage = [&](bool is_g1, int c, int t) -> bool {
+        const int s = st % L::NST;
+        if (st >= L::NST &&
+            !mbar_wait(&empty[s], ((st / L::NST) - 1) & 1, p.wc, abort_flag, SITE_MLP_PROD))
+          return false;
+        uint8_t *dst = smem + L::OFF_RING + s * STAGE_BYTES;
+        if (is_g1) {  // X [rows][k tile] 16 KB + W1 [k tile][chunks c, c+CS] 2 x 8 KB
+          mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+          tma_load_2d(dst, &tmX, &full[s], t * KT, rb * BM);
+          tma_load_2d(dst + 16384, &tmW1, &full[s], c * HC2, t * KT);
+          tma_load_2d(dst + 24576, &tmW1, &full[s], (c + CS) * HC2, t * KT);
+        } else {      // W2 [hidden 64][out 256q..] as 4 boxes of 64 columns
+          mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            tma_load_2d(dst + i * 8192, &tmW2, &full[s], q * BP + i * 64, c * HC2);
+        }
+        ++st;
+        return true;
+      };
+      if (n_pair >= 1)
+        for (int t = 0; t < NKT && ok; ++t) ok = stage(true, q, t);
+      for (int c = 0; c < NC && ok; ++c) {
+        if (c % (2 * CS) == q && c + 2 * CS < NC)
+          for (int t = 0; t < NKT && ok; ++t) ok = stage(true, c + 2 * CS, t);
+        if (ok) ok = stage(false, c, 0);
+      }
+      if (*abort_flag) {
+        for (int j = (st > L::NST ? st - L::NST : 0); j < st; ++j)
+          drain_wait(&full[j % L::NST], (j / L::NST) & 1, p.wc);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------ MMA issuer
+    {
+      const uint32_t id1 = idesc_bf16_f32(BM, 2 * HC2, 0, 1);  // T = X W1 (a pair), W1 MN-major
+      const uint32_t id2 = idesc_bf16_f32(BM, BP, 0, 1);   // O += H W2, W2 MN-major
+      const uint32_t ring = smem_u32(smem + L::OFF_RING);
+      int st = 0;
+      bool ok = true;
+      auto gemm1 = [&](int j) -> bool {  // own pair j into T buffer j & 1
+        const int b = j & 1;
+        if (j >= 2 && !mbar_wait_warp(&t_free[b], ((j >> 1) - 1) & 1, p.wc, abort_flag, SITE_MLP_MMA))
+          return false;
+        for (int t = 0; t < NKT; ++t, ++st) {
+          const int s = st % L::NST;
+          if (!mbar_wait_warp(&full[s], (st / L::NST) & 1, p.wc, abort_flag, SITE_MLP_MMA)) return false;
+          tc_fence_after();
+          const SDesc ax = sdesc_make(ring + s * STAGE_BYTES, 16, 1024);
+          const SDesc bw = sdesc_make(ring + s * STAGE_BYTES + 16384, 8192, 1024);
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < KT / 16; ++kk)
+              umma_f16_ss(tmem + b * 2 * HC2, sdesc_at(ax, kk * 32), sdesc_at(bw, kk * 2048), id1,
+                          (t > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&empty[s]);
+          }
+          __syncwarp();
+        }
+        if (elect_one()) umma_commit(&t_full[b]);
+        __syncwarp();
+        return true;
+      };
+      int pair = 0;
+      if (n_pair >= 1) ok = gemm1(pair++);
+      for (int c = 0; c < NC && ok; ++c) {
+        if (c % (2 * CS) == q && c + 2 * CS < NC && !(ok = gemm1(pair++))) break;
+        // GEMM2 of chunk c from slot k = its owner
+        const int k = c % CS, u = c / CS;
+        if (k != q && elect_one()) mbar_arrive_expect_tx(&h_full[k], L::SLOT_BYTES);
+        __syncwarp();
+        if (!mbar_wait_warp(&h_full[k], u & 1, p.wc, abort_flag, SITE_MLP_MMA)) {
+          ok = false;
+          break;
+        }
+        const int s = st % L::NST;
+        if (!mbar_wait_warp(&full[s], (st / L::NST) & 1, p.wc, abort_flag, SITE_MLP_MMA)) {
+          ok = false;
+          break;
+        }
+        ++st;
+        tc_fence_after();
+        const SDesc bw = sdesc_make(ring + s * STAGE_BYTES, 8192, 1024);
+        const SDesc dhi = sdesc_make(slot0 + k * L::SLOT_BYTES, 16, 1024);
+        const SDesc dlo = sdesc_make(slot0 + k * L::SLOT_BYTES + 16384, 16, 1024);
+        if (elect_one()) {
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int kk = 0; kk < HC2 / 16; ++kk)
+              umma_f16_ss(tmem + 256, sdesc_at(part ? dlo : dhi, kk * 32), sdesc_at(bw, kk * 2048),
+                          id2, (c > 0 || part > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&empty[s]);
+          umma_commit_multicast(&h_empty[k], (uint16_t)(1u << k));  // slot k read here
+        }
+        __syncwarp();
+      }
+      if (elect_one()) {
+        if (ok) umma_commit(o_done);
+        umma_commit(mma_drain);
+      }
+      __syncwarp();
+      if (lane == 0) drain_wait(mma_drain, 0, p.wc);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------- epilogue
+    // Every thread passes the same named barriers in every iteration; after
+    // a failure (abort flag) the waits and copies are skipped, not the loop.
+    const int row = threadIdx.x;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t my_hi = slot0 + q * L::SLOT_BYTES, my_lo = my_hi + 16384;
+    const bool issuer = threadIdx.x == 0;
+    bool ok = true;
+    for (int i = 0; i < n_own; ++i) {
+      const int j = i >> 1, h = i & 1, b = j & 1;  // pair j, half h, T buffer b
+      if (ok && h == 0) ok = mbar_wait(&t_full[b], (j >> 1) & 1, p.wc, abort_flag, SITE_MLP_EPI);
+      tc_fence_after();
+      uint32_t v[HC2];
+      const uint32_t tcol = tmem + lane_off + b * 2 * HC2 + h * HC2;
+      tmem_ld32(tcol, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(tcol + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      if (h == 1 || i == n_own - 1) mbar_arrive(&t_free[b]);  // both halves of the pair read
+      uint32_t hi[HC2 / 2], lo[HC2 / 2];
+#pragma unroll
+      for (int k = 0; k < HC2; k += 2) {
+        float h0 = __uint_as_float(v[k]), h1 = __uint_as_float(v[k + 1]);
+        if (p.gelu) {
+          h0 = gelu_tanh(h0);
+          h1 = gelu_tanh(h1);
+        }
+        const uint32_t ph = pack_bf16(h0, h1);
+        hi[k / 2] = ph;
+        lo[k / 2] = pack_bf16(h0 - __uint_as_float(ph << 16), h1 - __uint_as_float(ph & 0xffff0000u));
+      }
+      // slot q may be overwritten once every CTA has run GEMM2 on the
+      // previous own chunk and this CTA's copies of it have read the slot
+      if (issuer && ok) {
+        if (i >= 1) ok = mbar_wait(&h_empty[q], (i - 1) & 1, p.wc, abort_flag, SITE_MLP_EPI);
+        bulk_wait_read_all();
+      }
+      named_bar_sync(1, 128);
+      if (*abort_flag) ok = false;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint32_t off = sw128_off(row, ch);
+        st_shared_v4(my_hi + off, hi[4 * ch], hi[4 * ch + 1], hi[4 * ch + 2], hi[4 * ch + 3]);
+        st_shared_v4(my_lo + off, lo[4 * ch], lo[4 * ch + 1], lo[4 * ch + 2], lo[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (issuer && ok) {
+        mbar_arrive(&h_full[q]);  // own GEMM2 reads the slot in place
+        for (int r = 0; r < CS; ++r)
+          if (r != q)
+            bulk_copy_to_cluster(mapa_shared(my_hi, (uint32_t)r), my_hi, L::SLOT_BYTES,
+                                 mapa_shared(smem_u32(&h_full[q]), (uint32_t)r));
+        bulk_commit_group();
+      }
+    }
+    // O epilogue
+    if (ok && mbar_wait(o_done, 0, p.wc, abort_flag, SITE_MLP_EPI)) {
+      tc_fence_after();
+      __nv_bfloat16 *orow = p.O + (int64_t)(rb * BM + row) * p.P + q * BP;
+#pragma unroll 1
+      for (int j = 0; j < BP / 32; ++j) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + 256 + j * 32, r);
+        tmem_wait_ld();
+        uint4 *dst = reinterpret_cast<uint4 *>(orow + j * 32);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint4 o;
+          o.x = pack_bf16(__uint_as_float(r[8 * k + 0]), __uint_as_float(r[8 * k + 1]));
+          o.y = pack_bf16(__uint_as_float(r[8 * k + 2]), __uint_as_float(r[8 * k + 3]));
+          o.z = pack_bf16(__uint_as_float(r[8 * k + 4]), __uint_as_float(r[8 * k + 5]));
+          o.w = pack_bf16(__uint_as_float(r[8 * k + 6]), __uint_as_float(r[8 * k + 7]));
+          dst[k] = o;
+        }
+      }
+    }
+    // Before leaving: the outgoing copies have completed, and every CTA has
+    // run GEMM2 on this CTA's last chunk (the last h_empty phase, one phase
+    // after the one waited for above), so no peer signals this CTA any more.
+    if (issuer) {
+      bulk_wait_all();
+      if (n_own >= 1) {
+        volatile int never = 0;
+        mbar_wait(&h_empty[q], (n_own - 1) & 1, p.wc, &never, SITE_MLP_DRAIN);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_mlp_chain(const MlpArgs &a, const WaitCfg &wc, cudaStream_t st) {
@@ -365,6 +684,33 @@ cudaError_t launch_mlp_chain(const MlpArgs &a, const WaitCfg &wc, cudaStream_t s
     const uint64_t s[1] = {(uint64_t)a.P * 2};
     const uint32_t box[2] = {64, 64};
     if ((e = make_tmap(&mw2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.W2, d, s, box))) return e;
+  }
+  const int CS = a.P / BP;
+  if (CS >= 2 && CS <= MAX_CS && a.N % HC2 == 0) {
+    // X W1 once per row block, shared through the cluster
+    ClusterParams p;
+    p.M = a.M; p.K = a.K; p.N = a.N; p.P = a.P; p.gelu = a.gelu; p.CS = CS;
+    p.O = static_cast<__nv_bfloat16 *>(a.O);
+    p.wc = wc;
+    if ((e = cudaFuncSetAttribute(mlp_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  ClusterLayout::ALLOC)))
+      return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((a.M / BM) * CS));
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = ClusterLayout::ALLOC;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    timing_mark(st, 0);
+    e = cudaLaunchKernelEx(&cfg, mlp_cluster_kernel, mx, mw1, mw2, p);
+    timing_mark(st, 1);
+    return e != cudaSuccess ? e : cudaGetLastError();
   }
   MlpParams p;
   p.M = a.M;
