@@ -261,7 +261,7 @@ class HotPath:
         if self.mlp_ok:
             comps.append(dict(name="gelu_mlp_4096x1024x4096x1024",
                               flops=mlp_flops(m["M"], m["K"], m["N"], m["P"]), bytes=0.0, launches=1,
-                              kernels=[("mlp_chain_kernel", mlp_flops(m["M"], m["K"], m["N"], m["P"]),
+                              kernels=[("mlp_cluster_kernel", mlp_flops(m["M"], m["K"], m["N"], m["P"]),
                                         0.0)],
                               fn=lambda: cg.chain_fwd(self.x, self.w1, self.w2, cg.F_GELU_TANH, 0, 1.0,
                                                       self.o2, None)))
