@@ -71,6 +71,7 @@ struct BwdLayout {
 
 struct BwdParams {
   int BH, n, nb, causal;
+  int G;  // query heads per K/V head (grouped-query attention; 1 = none)
   float scale, scale_log2;
   const float *LSE;   // [BH][n]
   const float *Dvec;  // [BH][n]
@@ -185,12 +186,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // head-major order: the key blocks of one head run together and share Q,
-  // dO, LSE and D through L2; smallest (heaviest causal) block first
-  const int bh = blockIdx.x / p.nb;
+  // head-major order: the key blocks of one K/V head run together and share
+  // Q, dO, LSE and D through L2; smallest (heaviest causal) block first.
+  // Tile t covers query tile i_begin + t % Tq of query head bkv*G + t / Tq
+  // (Tq = nb - i_begin):
+  // with grouped-query attention dK and dV sum over the group's heads.
+  const int bkv = blockIdx.x / p.nb;
   const int jb = blockIdx.x % p.nb;
   const int i_begin = p.causal ? jb : 0;
-  const int T = p.nb - i_begin;
+  const int T = (p.nb - i_begin) * p.G;
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 16; ++b)
@@ -221,11 +225,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_arrive_expect_tx(kv_full, 2 * L::T_BYTES);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(smem + L::A_K + c * (BM * 128), &tmK, kv_full, c * 64, jb * BM, bh);
-        tma_load_3d(smem + L::A_V + c * (BM * 128), &tmV, kv_full, c * 64, jb * BM, bh);
+        tma_load_3d(smem + L::A_K + c * (BM * 128), &tmK, kv_full, c * 64, jb * BM, bkv);
+        tma_load_3d(smem + L::A_V + c * (BM * 128), &tmV, kv_full, c * 64, jb * BM, bkv);
       }
-      for (int t = 0; t < T; ++t) {
-        const int i = i_begin + t, s = t & 1;
+      int i = i_begin, bh = bkv * p.G;  // query tile and head of tile t
+      for (int t = 0; t < T; ++t, (++i == p.nb) ? (i = i_begin, ++bh) : 0) {
+        const int s = t & 1;
         if (t >= 2 && !mbar_wait(&q_empty[s], ((t >> 1) - 1) & 1, p.wc, abort_flag, SITE_BWD_PROD))
           break;
         mbar_arrive_expect_tx(&q_full[s], L::T_BYTES);
@@ -370,17 +375,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float *wd = sDv + w * 64;
     // LSE (log2 units) and D of query 64w + r of a tile (r < 64), fetched
     // one tile ahead
-    auto fetch = [&](int i, float &lv, float &dv) {
+    auto fetch = [&](int i, int bh, float &lv, float &dv) {
       const int q = i * BM + 64 * w + r;
       const bool q_ok = r < 64 && q < p.n;
       lv = q_ok ? __ldg(p.LSE + (int64_t)bh * p.n + q) * 1.4426950408889634f : INFINITY;
       dv = q_ok ? __ldg(p.Dvec + (int64_t)bh * p.n + q) : 0.0f;
     };
     float l_next = INFINITY, d_next = 0.0f;
-    if (T > 0) fetch(i_begin, l_next, d_next);
+    if (T > 0) fetch(i_begin, bkv * p.G, l_next, d_next);
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
-      const int i = i_begin + t;
+    int i = i_begin, bh = bkv * p.G;  // query tile and head of tile t
+    for (int t = 0; t < T; ++t, (++i == p.nb) ? (i = i_begin, ++bh) : 0) {
       const bool diag = p.causal && (i == jb);
       if (t > 0) named_bar_sync(1 + w, 128);  // warpgroup done with the staged values of t-1
       if (r < 64) {
@@ -388,7 +393,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         wd[r] = d_next;
       }
       named_bar_sync(1 + w, 128);
-      if (t + 1 < T) fetch(i + 1, l_next, d_next);
+      if (t + 1 < T) {
+        const bool wrap = i + 1 == p.nb;
+        fetch(wrap ? i_begin : i + 1, wrap ? bh + 1 : bh, l_next, d_next);
+      }
       if (ok) ok = mbar_wait(s_full, t & 1, p.wc, abort_flag, SITE_BWD_COMPUTE);
       tc_fence_after();
       // P^T for queries [64w, 64w+64): fp32 exponentials; S^T is released
@@ -458,7 +466,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok && T > 0 && mbar_wait(fin, 0, p.wc, abort_flag, SITE_BWD_EPI)) {
       tc_fence_after();
       // warpgroup 0 writes dV, warpgroup 1 writes dK (times scale)
-      __nv_bfloat16 *row = (w ? p.dK : p.dV) + ((int64_t)bh * p.n + kv_idx) * D;
+      __nv_bfloat16 *row = (w ? p.dK : p.dV) + ((int64_t)bkv * p.n + kv_idx) * D;
       store_row_bf16<D>((w ? tdK : tdV) + lane_off, row, w ? p.scale : 1.0f, kv_ok);
     }
   }
@@ -533,6 +541,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       int k_issued = 0, v_issued = 0;
+      const int bkv = bh / p.G;  // the group's K/V head
       for (int j = 0; j < NJ; ++j) {
         const int sk = j % 3;
         if (j >= 3 && !mbar_wait(&k_empty[sk], ((j / 3) - 1) & 1, p.wc, abort_flag, SITE_DQ_PROD))
@@ -541,7 +550,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(smem + L::B_K + sk * L::T_BYTES + c * (BM * 128), &tmK, &k_full[sk], c * 64,
-                      j * BM, bh);
+                      j * BM, bkv);
         k_issued = j + 1;
         if (j >= 3 && !mbar_wait(&v_empty[sk], ((j / 3) - 1) & 1, p.wc, abort_flag, SITE_DQ_PROD))
           break;
@@ -549,7 +558,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(smem + L::B_V + sk * L::T_BYTES + c * (BM * 128), &tmV, &v_full[sk], c * 64,
-                      j * BM, bh);
+                      j * BM, bkv);
         v_issued = j + 1;
       }
       if (*abort_flag) {
@@ -770,16 +779,18 @@ cudaError_t launch_bwd_d(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t s
   CUtensorMap mq, mk, mv, mdo;
   const uint32_t box[3] = {64, 128, 1};
   const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.n, (uint64_t)a.BH};
+  const uint64_t dkv[3] = {(uint64_t)D, (uint64_t)a.n, (uint64_t)a.BHkv};
   const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)a.n * D * 2};
   if ((e = make_tmap(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.Q, dims, str, box))) return e;
-  if ((e = make_tmap(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.K, dims, str, box))) return e;
-  if ((e = make_tmap(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.V, dims, str, box))) return e;
+  if ((e = make_tmap(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.K, dkv, str, box))) return e;
+  if ((e = make_tmap(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.V, dkv, str, box))) return e;
   if ((e = make_tmap(&mdo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.dO, dims, str, box))) return e;
   BwdParams p;
   p.BH = a.BH;
   p.n = a.n;
   p.nb = (a.n + BM - 1) / BM;
   p.causal = a.causal;
+  p.G = a.BH / a.BHkv;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.LSE = a.LSE;
@@ -796,12 +807,12 @@ cudaError_t launch_bwd_d(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t s
     return e;
   if ((e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, L::B_ALLOC)))
     return e;
-  const unsigned grid = (unsigned)(p.nb * a.BH);
+  const unsigned grid_kv = (unsigned)(p.nb * a.BHkv), grid_q = (unsigned)(p.nb * a.BH);
   timing_mark(st, 0);
-  ka<<<grid, NTHREADS, L::A_ALLOC, st>>>(mq, mk, mv, mdo, p);
+  ka<<<grid_kv, NTHREADS, L::A_ALLOC, st>>>(mq, mk, mv, mdo, p);
   timing_mark(st, 1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  kb<<<grid, NTHREADS, L::B_ALLOC, st>>>(mk, mv, p);
+  kb<<<grid_q, NTHREADS, L::B_ALLOC, st>>>(mk, mv, p);
   timing_mark(st, 2);
   return cudaGetLastError();
 }

@@ -61,6 +61,7 @@ struct FwdLayout {
 
 struct FwdParams {
   int BH, n, nqb2, nkb, causal;
+  int G;      // query heads per K/V head (grouped-query attention; 1 = none)
   int n_loc;  // positions per sequence shard (n when unsharded)
   float scale_log2;
   __nv_bfloat16 *O;
@@ -173,21 +174,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // 128-row box starting at sequence position `row`; over sequence
       // shards: shard row / n_loc, row row % n_loc in it (a box never
       // crosses a shard)
-      auto load = [&](uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int c0, int row) {
+      // Q of head bh; K and V of its group's head bh / G
+      auto load = [&](uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int c0, int row,
+                      int head) {
         if constexpr (SHARDED) {
           const int sh = row / p.n_loc;
-          tma_load_4d(dst, map, bar, c0, row - sh * p.n_loc, sh, bh);
+          tma_load_4d(dst, map, bar, c0, row - sh * p.n_loc, sh, head);
         } else {
-          tma_load_3d(dst, map, bar, c0, row, bh);
+          tma_load_3d(dst, map, bar, c0, row, head);
         }
       };
+      const int bkv = bh / p.G;
       mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
 #pragma unroll
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           load(smem + L::OFF_Q + t * L::Q_BYTES + c * (BM * 128), &tmQ, q_full, c * 64,
-               (2 * qb + t) * BM);
+               (2 * qb + t) * BM, bh);
       for (int j = 0; j < nkv_b; ++j) {
         const int st = j % STAGES;
         if (j >= STAGES &&
@@ -197,7 +201,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           load(smem + L::OFF_K + st * L::KV_BYTES + c * (BN * 128), &tmK, &k_full[st], c * 64,
-               j * BN);
+               j * BN, bkv);
         k_issued = j + 1;
         if (j >= STAGES &&
             !mbar_wait(&v_empty[st], ((j / STAGES) - 1) & 1, p.wc, abort_flag, SITE_FWD_PROD))
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           load(smem + L::OFF_V + st * L::KV_BYTES + c * (BN * 128), &tmV, &v_full[st], c * 64,
-               j * BN);
+               j * BN, bkv);
         v_issued = j + 1;
       }
       if (*abort_flag) {
@@ -459,11 +463,13 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t s
   const int nsh = a.n / a.n_loc;
   const uint32_t box[4] = {64, 128, 1, 1};
   uint64_t dims[4] = {(uint64_t)a.d, (uint64_t)a.n_loc, (uint64_t)nsh, (uint64_t)a.BH};
+  uint64_t dkv[4] = {(uint64_t)a.d, (uint64_t)a.n_loc, (uint64_t)nsh, (uint64_t)a.BHkv};
   uint64_t sq[3] = {(uint64_t)a.q_srow * 2, (uint64_t)a.q_sshard * 2, (uint64_t)a.q_sbh * 2};
   uint64_t sk[3] = {(uint64_t)a.k_srow * 2, (uint64_t)a.k_sshard * 2, (uint64_t)a.k_sbh * 2};
   uint64_t sv[3] = {(uint64_t)a.v_srow * 2, (uint64_t)a.v_sshard * 2, (uint64_t)a.v_sbh * 2};
   if (!sharded) {  // drop the shard dimension
     dims[2] = dims[3];
+    dkv[2] = dkv[3];
     sq[1] = sq[2];
     sk[1] = sk[2];
     sv[1] = sv[2];
@@ -471,9 +477,9 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t s
   cudaError_t e;
   if ((e = make_tmap(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, a.Q, dims, sq, box)) != cudaSuccess)
     return e;
-  if ((e = make_tmap(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, a.K, dims, sk, box)) != cudaSuccess)
+  if ((e = make_tmap(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, a.K, dkv, sk, box)) != cudaSuccess)
     return e;
-  if ((e = make_tmap(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, a.V, dims, sv, box)) != cudaSuccess)
+  if ((e = make_tmap(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, a.V, dkv, sv, box)) != cudaSuccess)
     return e;
   FwdParams p;
   p.BH = a.BH;
@@ -487,6 +493,7 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t s
   p.o_srow = a.o_srow;
   p.o_sshard = a.o_sshard;
   p.n_loc = a.n_loc;
+  p.G = a.BH / a.BHkv;
   p.LSE = a.LSE;
   p.lse_sbh = a.lse_sbh;
   p.wc = wc;

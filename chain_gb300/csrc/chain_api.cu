@@ -144,6 +144,13 @@ bool same_shape(const View &a, const View &b) {
   return a.outer == b.outer && a.rows == b.rows && a.cols == b.cols;
 }
 
+// K or V of grouped-query attention for queries q: the same [n][d] rows and
+// a head count that divides q's (each K/V head serves q.outer / kv.outer
+// consecutive query heads).
+bool kv_shape(const View &q, const View &kv) {
+  return kv.rows == q.rows && kv.cols == q.cols && kv.outer >= 1 && q.outer % kv.outer == 0;
+}
+
 // LSE [BH][n] (2-D), or [B][H][n] (3-D) folded, innermost contiguous.
 int lse_view(const chain_tensor_t *t, int64_t BH, int64_t n, int64_t *s_bh) {
   if (!t || !t->ptr) return CHAIN_ERR_ARG;
@@ -281,7 +288,7 @@ int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B, const chain_tens
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   if (f == CHAIN_F_SOFTMAX) {
-    if (!same_shape(a, b) || !same_shape(a, c) || !same_shape(a, o)) return CHAIN_ERR_ARG;
+    if (!kv_shape(a, b) || !same_shape(b, c) || !same_shape(a, o)) return CHAIN_ERR_ARG;
     if (a.cols != 64 && a.cols != 128) return CHAIN_ERR_ARG;
     if (a.rows < 1 || a.outer < 1) return CHAIN_ERR_ARG;
     if (a.rows > (1 << 30) || a.outer > 65535 * 16) return CHAIN_ERR_ARG;
@@ -297,6 +304,7 @@ int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B, const chain_tens
     args.O = o.ptr; args.o_sbh = o.s_outer; args.o_srow = o.s_row;
     args.LSE = static_cast<float *>(LSE->ptr); args.lse_sbh = lse_sbh;
     args.BH = (int)a.outer; args.n = (int)a.rows; args.d = (int)a.cols;
+    args.BHkv = (int)b.outer;
     args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
     args.n_loc = args.n;
     args.q_sshard = args.k_sshard = args.v_sshard = args.o_sshard = 0;
@@ -306,7 +314,7 @@ int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B, const chain_tens
     if (a.dtype == CHAIN_BF16) {
       e = launch_attn_fwd_bf16(args, wait_cfg(di), st);
     } else {
-      if (a.cols != 64) return CHAIN_ERR_UNSUPPORTED;
+      if (a.cols != 64 || b.outer != a.outer) return CHAIN_ERR_UNSUPPORTED;
       e = launch_attn_fwd_f32(args, wait_cfg(di), st);
     }
     if (e == cudaErrorNotSupported) return CHAIN_ERR_UNSUPPORTED;
@@ -345,7 +353,7 @@ static size_t mlp_ws_bytes(const View &a, const View &c) {
 size_t chain_bwd_workspace_size(const chain_tensor_t *A, const chain_tensor_t *C) {
   View a, c;
   if (view_of(A, 2, &a) || view_of(C, 2, &c)) return 0;
-  if (!same_shape(a, c)) {
+  if (!kv_shape(a, c)) {
     // different shapes: the MLP chain (A = X [M][K], C = W2 [N][P])
     if (A->ndim != 2 || C->ndim != 2) return 0;
     return mlp_ws_bytes(a, c);
@@ -357,7 +365,7 @@ size_t chain_bwd_workspace_size(const chain_tensor_t *A, const chain_tensor_t *C
 size_t chain_bwd_workspace_size_f(const chain_tensor_t *A, const chain_tensor_t *C, int f) {
   if (f == CHAIN_F_SOFTMAX) {
     View a, c;
-    if (view_of(A, 2, &a) || view_of(C, 2, &c) || !same_shape(a, c)) return 0;
+    if (view_of(A, 2, &a) || view_of(C, 2, &c) || !kv_shape(a, c)) return 0;
     return ((size_t)a.outer * a.rows * sizeof(float) + 255) & ~size_t(255);
   }
   if (f != CHAIN_F_IDENTITY && f != CHAIN_F_GELU_TANH) return 0;
@@ -419,7 +427,9 @@ int chain_bwd(const chain_tensor_t *dO, const chain_tensor_t *A, const chain_ten
   const View *all[8] = {&g, &q, &k, &v, &o, &dq, &dk, &dv};
   for (const View *x : all) {
     if (x->dtype != CHAIN_BF16) return CHAIN_ERR_DTYPE;
-    if (!same_shape(*x, q)) return CHAIN_ERR_ARG;
+    // Q, dO, O, dQ of one shape; K, V, dK, dV of one (grouped-query) shape
+    const bool kv_side = x == &k || x == &v || x == &dk || x == &dv;
+    if (kv_side ? !(kv_shape(q, *x) && same_shape(*x, k)) : !same_shape(*x, q)) return CHAIN_ERR_ARG;
     // the backward kernels take densely packed [BH][n][d]
     if (x->s_row != x->cols || (x->outer > 1 && x->s_outer != x->rows * x->cols))
       return CHAIN_ERR_ARG;
@@ -439,6 +449,7 @@ int chain_bwd(const chain_tensor_t *dO, const chain_tensor_t *A, const chain_ten
   args.dQ = dq.ptr; args.dK = dk.ptr; args.dV = dv.ptr;
   args.Dvec = static_cast<float *>(workspace);
   args.BH = (int)q.outer; args.n = (int)q.rows; args.d = (int)q.cols;
+  args.BHkv = (int)k.outer;
   args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
   DevInfo *di = nullptr;
   if ((rc = device_ready(&di))) return rc;
@@ -518,7 +529,8 @@ int chain_fwd_sp(const chain_tensor_t *Q, const chain_tensor_t *K, const chain_t
   args.v_sbh = V->stride[2]; args.v_srow = V->stride[1]; args.v_sshard = V->stride[0];
   args.o_sbh = O->stride[2]; args.o_srow = O->stride[1]; args.o_sshard = O->stride[0];
   args.LSE = static_cast<float *>(LSE->ptr); args.lse_sbh = lse_sbh;
-  args.BH = (int)Hl; args.n = (int)n; args.d = (int)d; args.n_loc = (int)n_loc;
+  args.BH = (int)Hl; args.BHkv = (int)Hl; args.n = (int)n; args.d = (int)d;
+  args.n_loc = (int)n_loc;
   args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
   DevInfo *di = nullptr;
   if ((rc = device_ready(&di))) return rc;

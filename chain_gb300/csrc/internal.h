@@ -23,6 +23,7 @@ struct AttnFwdArgs {
   float *LSE;
   int64_t lse_sbh;
   int BH, n, d, causal;
+  int BHkv;  // K/V heads; BH / BHkv query heads share each (grouped-query attention)
   float scale;
   // Sequence split into n / n_loc shards: position s*n_loc + t lives at
   // s*x_sshard + t*x_srow (elements).  n_loc = n for one contiguous run.
@@ -34,11 +35,12 @@ cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs &a, const WaitCfg &wc, cudaSt
 cudaError_t launch_attn_fwd_f32(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t st);
 
 struct AttnBwdArgs {
-  const void *Q, *K, *V, *O, *dO;  // bf16 [BH][n][d], row stride d, head stride n*d
+  const void *Q, *K, *V, *O, *dO;  // bf16 [BH][n][d] (K, V: [BHkv][n][d]), row stride d
   const float *LSE;                // [BH][n]
-  void *dQ, *dK, *dV;              // bf16 [BH][n][d]
+  void *dQ, *dK, *dV;              // bf16, shaped as Q, K, V
   float *Dvec;                     // fp32 [BH][n] workspace
   int BH, n, d, causal;
+  int BHkv;  // K/V heads (grouped-query attention: BH / BHkv query heads each)
   float scale;
 };
 cudaError_t launch_attn_bwd(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t st);

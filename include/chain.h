@@ -83,6 +83,10 @@ typedef struct {
  * f = CHAIN_F_SOFTMAX (attention):
  *   A = Q [BH][n][d], B = K [BH][n][d] (passed untransposed; the product is
  *   Q K^T), C = V [BH][n][d]; 3-D, or 4-D [B][H][n][d] (B*H folded).
+ *   Grouped-query attention (bf16): K and V may have fewer heads, [BHkv][n][d]
+ *   with BH a multiple of BHkv; query head h then attends K/V head
+ *   h / (BH / BHkv) (for 4-D, H a multiple of Hkv keeps each group within
+ *   one batch entry).
  *   n >= 1.  bf16 in -> O bf16, d in {64, 128}; O is accumulated from the
  *   compensated pair P_hi + P_lo (bf16 head and residual of P) so the only
  *   bf16 rounding is the output's.  f32 in -> O f32, d = 64 only (else
@@ -126,7 +130,9 @@ size_t chain_bwd_workspace_size_f(const chain_tensor_t *A, const chain_tensor_t 
  *   Inputs: dO, Q (A), K (B), V (C), O [BH][n][d] bf16 and LSE [BH][n] f32
  *   as produced by chain_fwd with the same f, mask and scale.  Only
  *   f = CHAIN_F_SOFTMAX with bf16 and d in {64, 128} is supported.
- *   Outputs: dQ (dA), dK (dB), dV (dC) [BH][n][d] bf16.
+ *   Outputs: dQ (dA), dK (dB), dV (dC) [BH][n][d] bf16.  With grouped-query
+ *   attention K, V, dK, dV are [BHkv][n][d] and dK, dV sum over the query
+ *   heads of each group.
  *   S and P are recomputed per tile from LSE ("recompute, don't store",
  *   AutoSP 2.B); D_i = sum_e dO_ie O_ie.  dK, dV come from one pass over
  *   the key blocks and dQ from a second over the query tiles, each

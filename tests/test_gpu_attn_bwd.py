@@ -83,3 +83,25 @@ def test_bwd_rejects_small_workspace(cg):
     ws = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(cg.ChainError):
         cg.attention_bwd(q, q, q, q, q, lse, True, workspace=ws)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("BH,BHkv,n,d", [(8, 2, 256, 128), (6, 3, 300, 64), (4, 1, 129, 128)])
+def test_bwd_grouped_query_vs_oracle(cg, orc, BH, BHkv, n, d, causal):
+    # Grouped-query attention: the oracle sees K and V repeated over each
+    # group; dK and dV of a K/V head are the sums over its group.
+    q, _, _, do = cs.attn_inputs(BH, n, d, seed=7600 + BH + n, with_do=True)
+    _, k, v = cs.attn_inputs(BHkv, n, d, seed=7700 + BHkv + n)
+    G = BH // BHkv
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = cg.attention_fwd(qd, kd, vd, causal)
+    dq, dk, dv = cg.attention_bwd(dod, qd, kd, vd, o, lse, causal)
+    assert cg.chain_check()[0] == 0
+    assert dk.shape == k.shape and dv.shape == v.shape
+    rq, rk, rv, _ = orc.softmax_bwd(q, k.repeat_interleave(G, 0), v.repeat_interleave(G, 0), do,
+                                    d ** -0.5, causal)
+    rk = np.asarray(rk).reshape(BHkv, G, n, d).sum(1)
+    rv = np.asarray(rv).reshape(BHkv, G, n, d).sum(1)
+    assert_grad_close(dq, rq, "GQA dQ")
+    assert_grad_close(dk, rk, "GQA dK")
+    assert_grad_close(dv, rv, "GQA dV")

@@ -138,3 +138,26 @@ def test_fwd_fp32_rejects_d128(cg):
     with pytest.raises(cg.ChainError) as ei:
         cg.attention_fwd(q, q, q, False)
     assert ei.value.status == cg.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("BH,BHkv,n,d", [(8, 2, 300, 128), (6, 3, 256, 64), (4, 1, 129, 128)])
+def test_fwd_grouped_query_vs_oracle(cg, orc, BH, BHkv, n, d, causal):
+    # Grouped-query attention: query head h reads K/V head h // (BH // BHkv).
+    # The oracle sees K and V repeated over each group.
+    q, _, _ = cs.attn_inputs(BH, n, d, seed=7400 + BH + n)
+    _, k, v = cs.attn_inputs(BHkv, n, d, seed=7500 + BHkv + n)
+    G = BH // BHkv
+    o, lse = cg.attention_fwd(q.cuda(), k.cuda(), v.cuda(), causal)
+    assert cg.chain_check()[0] == 0
+    ro, rl = orc.softmax_fwd(q, k.repeat_interleave(G, 0), v.repeat_interleave(G, 0), d ** -0.5,
+                             causal)
+    assert_fwd_close(o, ro, f"GQA O {BH}/{BHkv}x{n}x{d}")
+    assert_lse_close(lse, rl, "GQA LSE")
+
+
+def test_fwd_grouped_query_bad_ratio(cg):
+    q = torch.zeros(6, 128, 128, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(4, 128, 128, dtype=torch.bfloat16, device="cuda")  # 6 % 4 != 0
+    with pytest.raises(cg.ChainError):
+        cg.attention_fwd(q, k, k, True)
