@@ -73,6 +73,7 @@ def _load():
             lib.chain_bwd_workspace_size_f.argtypes = [P, P, ci]
             lib.chain_bwd_workspace_size_f.restype = ctypes.c_size_t
             lib.chain_fwd_sp.argtypes = [P, P, P, ci, ci, ci, fl, P, P, vp]
+            lib.chain_fwd_varlen.argtypes = [P, P, P, vp, ci, ci, ci, fl, P, P, vp]
             lib.sp_relayout.argtypes = [P, ci, ci, P, vp]
             lib.sp_relayout_inverse.argtypes = [P, ci, ci, P, vp]
             lib.chain_check.argtypes = [vp, ctypes.POINTER(ci)]
@@ -84,7 +85,8 @@ def _load():
             lib.chain_umma_selftest.argtypes = [vp, vp, vp, ci, ci, ci, vp]
             lib.chain_status_string.argtypes = [ci]
             lib.chain_status_string.restype = ctypes.c_char_p
-            for fn in ("chain_fwd", "chain_fwd_sp", "chain_bwd", "chain_bwd_noalloc", "sp_relayout",
+            for fn in ("chain_fwd", "chain_fwd_sp", "chain_fwd_varlen", "chain_bwd", "chain_bwd_noalloc",
+                       "sp_relayout",
                        "sp_relayout_inverse",
                        "chain_check", "chain_selftest_wait_timeout", "chain_umma_selftest",
                        "chain_last_cuda_error"):
@@ -155,6 +157,17 @@ def chain_fwd_sp(Q, K, V, p, head_group, mask, scale, O, LSE, stream=None):
     _ok(_load().chain_fwd_sp(_ref(desc(Q)), _ref(desc(K)), _ref(desc(V)), int(p), int(head_group),
                              int(mask), float(scale), _ref(desc(O)), _ref(desc(LSE)),
                              _stream(stream)), "chain_fwd_sp")
+
+
+def chain_fwd_varlen(Q, K, V, cu_seqlens, batch, max_seqlen, mask, scale, O, LSE, stream=None):
+    """Attention over sequences packed end to end; cu_seqlens is a device
+    int32 tensor [batch + 1]; see include/chain.h."""
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+        raise ValueError("cu_seqlens must be a CUDA int32 tensor")
+    _ok(_load().chain_fwd_varlen(_ref(desc(Q)), _ref(desc(K)), _ref(desc(V)),
+                                 ctypes.c_void_p(cu_seqlens.data_ptr()), int(batch), int(max_seqlen),
+                                 int(mask), float(scale), _ref(desc(O)), _ref(desc(LSE)),
+                                 _stream(stream)), "chain_fwd_varlen")
 
 
 def chain_bwd_workspace_size(A, C) -> int:
@@ -248,6 +261,18 @@ def attention_fwd_sp(q, k, v, p: int, head_group: int, causal: bool, scale: floa
         o = torch.zeros_like(q)
     lse = torch.empty(H // p, p * n_loc, dtype=torch.float32, device=q.device)
     chain_fwd_sp(q, k, v, p, head_group, MASK_CAUSAL if causal else MASK_NONE, scale, o, lse, stream)
+    return o, lse
+
+
+def attention_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool,
+                         scale: float | None = None, stream=None):
+    """q [total, H, d], k, v [total, Hkv, d]; cu_seqlens a CUDA int32 tensor
+    [batch + 1].  Returns (O [total, H, d], LSE [H, total])."""
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=q.device)
+    chain_fwd_varlen(q, k, v, cu_seqlens, cu_seqlens.numel() - 1, max_seqlen,
+                     MASK_CAUSAL if causal else MASK_NONE, scale, o, lse, stream)
     return o, lse
 
 

@@ -62,6 +62,11 @@ struct FwdLayout {
 struct FwdParams {
   int BH, n, nqb2, nkb, causal;
   int G;      // query heads per K/V head (grouped-query attention; 1 = none)
+  // Variable-length batch (null cu when not): sequence b occupies rows
+  // [cu[b], cu[b+1]) of the packed tensors; CTAs run per (head, sequence,
+  // 256-row block) over nqb2 blocks of the longest sequence.
+  const int *cu;
+  int nbatch;
   int n_loc;  // positions per sequence shard (n when unsharded)
   float scale_log2;
   __nv_bfloat16 *O;
@@ -97,13 +102,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 
 // Number of key tiles query tile t (0 = a, 1 = b) of 256-row block qb sees.
-__device__ __forceinline__ int kv_tiles(const FwdParams &p, int qb, int t) {
-  if (!p.causal) return p.nkb;
+__device__ __forceinline__ int kv_tiles(const FwdParams &p, int nkb, int qb, int t) {
+  if (!p.causal) return nkb;
   const int last = 2 * qb + t + 1;  // tiles 0..2qb+t hold keys <= the tile's rows
-  return last < p.nkb ? last : p.nkb;
+  return last < nkb ? last : nkb;
 }
 
-template <int D, bool SHARDED>
+template <int D, bool SHARDED, bool VARLEN>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
@@ -131,10 +136,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // Head-major order: the CTAs resident at one time cover one or two heads,
   // whose K and V then stay in L2 for every query block that reads them;
   // within a head the heaviest (last) causal blocks go first.
-  const int bh = blk / p.nqb2;
-  const int qb = p.causal ? (p.nqb2 - 1 - blk % p.nqb2) : (blk % p.nqb2);
-  const int nkv_a = kv_tiles(p, qb, 0);
-  const int nkv_b = kv_tiles(p, qb, 1);
+  int bh, qb, n = p.n, row0 = 0;
+  if constexpr (!VARLEN) {
+    bh = blk / p.nqb2;
+    qb = p.causal ? (p.nqb2 - 1 - blk % p.nqb2) : (blk % p.nqb2);
+  } else {
+    // one sequence of a variable-length batch; bounds clamped to the packed
+    // tensor so a bad cu can never address memory outside it
+    const int per_head = p.nbatch * p.nqb2;
+    bh = blk / per_head;
+    const int b = (blk % per_head) / p.nqb2, k = blk % p.nqb2;
+    int lo = __ldg(p.cu + b), hi = __ldg(p.cu + b + 1);
+    lo = lo < 0 ? 0 : (lo > p.n ? p.n : lo);
+    hi = hi < lo ? lo : (hi > p.n ? p.n : hi);
+    row0 = lo;
+    n = hi - lo;
+    const int nqb2_b = (n + 2 * BM - 1) / (2 * BM);
+    if (nqb2_b > p.nqb2 && k == 0 && threadIdx.x == 0 && bh == 0)
+      atomicExch(&p.wc.status->reserved[0], 1);  // sequence longer than the stated maximum
+    if (k >= nqb2_b) return;  // nothing of this sequence for this CTA
+    qb = p.causal ? nqb2_b - 1 - k : k;
+  }
+  const int nkb = (n + BN - 1) / BN;
+  const int nkv_a = kv_tiles(p, nkb, qb, 0);
+  const int nkv_b = kv_tiles(p, nkb, qb, 1);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -181,7 +206,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int sh = row / p.n_loc;
           tma_load_4d(dst, map, bar, c0, row - sh * p.n_loc, sh, head);
         } else {
-          tma_load_3d(dst, map, bar, c0, row, head);
+          tma_load_3d(dst, map, bar, c0, row0 + row, head);
         }
       };
       const int bkv = bh / p.G;
@@ -339,7 +364,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_after();
       const int kv0 = j * BN;
       const bool diag = p.causal && (j == 2 * qb + t);
-      const bool masked = diag || (kv0 + BN > p.n);
+      const bool masked = diag || (kv0 + BN > n);
       // Row of S: one round trip to tensor memory, kept in registers for
       // both passes.  Diagonal and ragged tiles mask keys after the row and
       // keys beyond n.
@@ -352,7 +377,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int k = 0; k < BN; ++k) {
           const int kv = kv0 + k;
-          if ((diag && kv > q_idx) || kv >= p.n) s[k] = __float_as_uint(-INFINITY);
+          if ((diag && kv > q_idx) || kv >= n) s[k] = __float_as_uint(-INFINITY);
         }
       }
       // pass 1: row max, eight independent partial maxima (a tree, not a
@@ -420,13 +445,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float inv_l = 1.0f / l;
       const int q_sh = SHARDED ? q_idx / p.n_loc : 0;
       __nv_bfloat16 *orow = p.O + (int64_t)bh * p.o_sbh + (int64_t)q_sh * p.o_sshard +
-                            (int64_t)(q_idx - q_sh * p.n_loc) * p.o_srow;
+                            (int64_t)(row0 + q_idx - q_sh * p.n_loc) * p.o_srow;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(tO + c * 32, o);
         tmem_wait_ld();
-        if (q_idx < p.n) {
+        if (q_idx < n) {
           uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -439,8 +464,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
       }
-      if (q_idx < p.n)
-        p.LSE[(int64_t)bh * p.lse_sbh + q_idx] = (m + lg2(l)) * 0.69314718055994531f;
+      if (q_idx < n)
+        p.LSE[(int64_t)bh * p.lse_sbh + row0 + q_idx] = (m + lg2(l)) * 0.69314718055994531f;
     }
   }
 
@@ -484,7 +509,11 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t s
   FwdParams p;
   p.BH = a.BH;
   p.n = a.n;
-  p.nqb2 = (a.n + 2 * BM - 1) / (2 * BM);
+  p.cu = a.cu_seqlens;
+  p.nbatch = a.nbatch;
+  // with a variable-length batch, blocks per head come from the longest sequence
+  const int nmax = a.cu_seqlens ? a.max_seqlen : a.n;
+  p.nqb2 = (nmax + 2 * BM - 1) / (2 * BM);
   p.nkb = (a.n + BN - 1) / BN;
   p.causal = a.causal;
   p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -497,10 +526,11 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t s
   p.LSE = a.LSE;
   p.lse_sbh = a.lse_sbh;
   p.wc = wc;
-  auto kern = sharded ? attn_fwd_kernel<D, true> : attn_fwd_kernel<D, false>;
+  auto kern = sharded ? attn_fwd_kernel<D, true, false>
+                      : (a.cu_seqlens ? attn_fwd_kernel<D, false, true> : attn_fwd_kernel<D, false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(p.nqb2 * a.BH);
+  const unsigned grid = (unsigned)(p.nqb2 * a.BH * (a.cu_seqlens ? a.nbatch : 1));
   timing_mark(st, 0);
   kern<<<grid, NTHREADS, L::ALLOC, st>>>(mq, mk, mv, p);
   timing_mark(st, 1);

@@ -118,6 +118,9 @@ int view_of(const chain_tensor_t *t, int min_nd, View *v) {
   v->cols = t->shape[nd - 1];
   v->rows = nd >= 2 ? t->shape[nd - 2] : 1;
   v->s_row = nd >= 2 ? t->stride[nd - 2] : v->cols;
+  // the stride of a size-1 dimension is arbitrary (frameworks report any
+  // value there): use the canonical one
+  if (v->rows == 1) v->s_row = v->cols;
   if (nd <= 2) {
     v->outer = 1;
     v->s_outer = v->rows * v->s_row;
@@ -125,10 +128,12 @@ int view_of(const chain_tensor_t *t, int min_nd, View *v) {
     v->outer = t->shape[0];
     v->s_outer = t->stride[0];
   } else {
-    if (t->shape[1] > 1 && t->stride[0] != t->shape[1] * t->stride[1]) return CHAIN_ERR_ARG;
+    if (t->shape[0] > 1 && t->shape[1] > 1 && t->stride[0] != t->shape[1] * t->stride[1])
+      return CHAIN_ERR_ARG;
     v->outer = t->shape[0] * t->shape[1];
-    v->s_outer = t->stride[1];
+    v->s_outer = t->shape[1] > 1 ? t->stride[1] : t->stride[0];
   }
+  if (v->outer == 1) v->s_outer = v->rows * v->s_row;
   if (v->rows > 1 && v->s_row < v->cols) return CHAIN_ERR_ARG;
   if (v->outer > 1 && v->s_outer < v->rows * v->s_row) return CHAIN_ERR_ARG;
   return CHAIN_OK;
@@ -242,11 +247,12 @@ int chain_check(void *stream, int *detail) {
   e = cudaMemcpyFromSymbol(&hs, g_status, sizeof hs);
   if (e != cudaSuccess) return cuda_fail(e);
   if (detail) *detail = hs.site;
-  if (hs.timeout) {
+  if (hs.timeout || hs.reserved[0]) {
     DevStatus zero = {0, 0, {0, 0}};
     e = cudaMemcpyToSymbol(g_status, &zero, sizeof zero);
     if (e != cudaSuccess) return cuda_fail(e);
-    return CHAIN_ERR_TIMEOUT;
+    // a bounded wait expired, or a kernel met an argument only it could check
+    return hs.timeout ? CHAIN_ERR_TIMEOUT : CHAIN_ERR_ARG;
   }
   return CHAIN_OK;
 }
@@ -308,6 +314,7 @@ int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B, const chain_tens
     args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
     args.n_loc = args.n;
     args.q_sshard = args.k_sshard = args.v_sshard = args.o_sshard = 0;
+    args.cu_seqlens = nullptr; args.nbatch = 0; args.max_seqlen = 0;
     DevInfo *di = nullptr;
     if ((rc = device_ready(&di))) return rc;
     cudaError_t e;
@@ -531,7 +538,55 @@ int chain_fwd_sp(const chain_tensor_t *Q, const chain_tensor_t *K, const chain_t
   args.LSE = static_cast<float *>(LSE->ptr); args.lse_sbh = lse_sbh;
   args.BH = (int)Hl; args.BHkv = (int)Hl; args.n = (int)n; args.d = (int)d;
   args.n_loc = (int)n_loc;
+  args.cu_seqlens = nullptr; args.nbatch = 0; args.max_seqlen = 0;
   args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
+  DevInfo *di = nullptr;
+  if ((rc = device_ready(&di))) return rc;
+  cudaError_t e = launch_attn_fwd_bf16(args, wait_cfg(di), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
+}
+
+// Packed variable-length tensor [total][H][d] bf16: d contiguous, row and
+// head strides in 16-byte multiples, 16-byte aligned.
+static int packed_view(const chain_tensor_t *t, int64_t total, int64_t H, int64_t d) {
+  if (!t || !t->ptr || t->ndim != 3) return CHAIN_ERR_ARG;
+  if (t->dtype != CHAIN_BF16) return CHAIN_ERR_DTYPE;
+  if (t->shape[0] != total || t->shape[1] != H || t->shape[2] != d) return CHAIN_ERR_ARG;
+  if (t->stride[2] != 1 || !aligned16(t->ptr)) return CHAIN_ERR_ARG;
+  if (t->stride[0] <= 0 || t->stride[1] <= 0 || (t->stride[0] * 2) % 16 || (t->stride[1] * 2) % 16)
+    return CHAIN_ERR_ARG;
+  return CHAIN_OK;
+}
+
+int chain_fwd_varlen(const chain_tensor_t *Q, const chain_tensor_t *K, const chain_tensor_t *V,
+                     const int32_t *cu_seqlens, int batch, int max_seqlen, int mask, float scale,
+                     chain_tensor_t *O, chain_tensor_t *LSE, void *stream) {
+  if (!Q || Q->ndim != 3 || !K || K->ndim != 3) return CHAIN_ERR_ARG;
+  if (mask != CHAIN_MASK_NONE && mask != CHAIN_MASK_CAUSAL) return CHAIN_ERR_ARG;
+  const int64_t total = Q->shape[0], H = Q->shape[1], d = Q->shape[2], Hkv = K->shape[1];
+  int rc;
+  if ((rc = packed_view(Q, total, H, d)) || (rc = packed_view(K, total, Hkv, d)) ||
+      (rc = packed_view(V, total, Hkv, d)) || (rc = packed_view(O, total, H, d)))
+    return rc;
+  if (total < 1 || total > (1 << 30) || (d != 64 && d != 128)) return CHAIN_ERR_ARG;
+  if (Hkv < 1 || H % Hkv || H > 65535 * 16) return CHAIN_ERR_ARG;
+  if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return CHAIN_ERR_ARG;
+  if (batch < 1 || batch > (1 << 20) || max_seqlen < 1 || max_seqlen > total) return CHAIN_ERR_ARG;
+  if (!(scale > 0.0f) || !(scale < 1e30f)) return CHAIN_ERR_ARG;
+  int64_t lse_sbh = 0;
+  if ((rc = lse_view(LSE, H, total, &lse_sbh))) return rc;
+  AttnFwdArgs args;
+  args.Q = Q->ptr; args.K = K->ptr; args.V = V->ptr; args.O = O->ptr;
+  args.q_sbh = Q->stride[1]; args.q_srow = Q->stride[0];
+  args.k_sbh = K->stride[1]; args.k_srow = K->stride[0];
+  args.v_sbh = V->stride[1]; args.v_srow = V->stride[0];
+  args.o_sbh = O->stride[1]; args.o_srow = O->stride[0];
+  args.LSE = static_cast<float *>(LSE->ptr); args.lse_sbh = lse_sbh;
+  args.BH = (int)H; args.BHkv = (int)Hkv; args.n = (int)total; args.d = (int)d;
+  args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
+  args.n_loc = args.n;
+  args.q_sshard = args.k_sshard = args.v_sshard = args.o_sshard = 0;
+  args.cu_seqlens = cu_seqlens; args.nbatch = batch; args.max_seqlen = max_seqlen;
   DevInfo *di = nullptr;
   if ((rc = device_ready(&di))) return rc;
   cudaError_t e = launch_attn_fwd_bf16(args, wait_cfg(di), static_cast<cudaStream_t>(stream));

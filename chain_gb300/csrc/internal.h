@@ -29,6 +29,10 @@ struct AttnFwdArgs {
   // s*x_sshard + t*x_srow (elements).  n_loc = n for one contiguous run.
   int n_loc;
   int64_t q_sshard, k_sshard, v_sshard, o_sshard;
+  // Variable-length batch: device int32 [nbatch + 1] row offsets into the
+  // packed rows (n = total rows), or null.
+  const int *cu_seqlens;
+  int nbatch, max_seqlen;
 };
 
 cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t st);

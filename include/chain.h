@@ -225,6 +225,32 @@ int chain_fwd_sp(const chain_tensor_t *Q, const chain_tensor_t *K,
                  void *stream);
 
 /*
+ * chain_fwd_varlen -- softmax attention over a batch of sequences of
+ * different lengths packed end to end (the long-sequence regime of "Ulysses
+ * Sequence Parallelism", "Contexte Technique", batches sequences of uneven
+ * length; the unit is the O = f(A B) C of "Memory-efficient tensor
+ * parallelism", FITEE 10.1631/FITEE.2400602).  Each sequence attends to
+ * itself only.
+ *   Q, O        [total][H][d] bf16;  K, V  [total][Hkv][d] bf16 (Hkv divides
+ *               H: grouped-query attention as in chain_fwd); d = 64 or 128,
+ *               contiguous; row and head strides multiples of 16 bytes.
+ *   cu_seqlens  DEVICE int32 [batch + 1]: sequence b is rows
+ *               [cu_seqlens[b], cu_seqlens[b+1]); nondecreasing, last =
+ *               total.  Offsets are clamped to [0, total] on the device.
+ *   max_seqlen  at least the longest sequence; a longer sequence is not
+ *               computed and the next chain_check() returns CHAIN_ERR_ARG.
+ *   mask, scale as for chain_fwd with f = CHAIN_F_SOFTMAX (causal positions
+ *               count from each sequence's start).
+ *   LSE         [H][total] fp32, natural log.
+ * Rows of each sequence are computed exactly as chain_fwd computes that
+ * sequence alone.  Asynchronous on `stream`.
+ */
+int chain_fwd_varlen(const chain_tensor_t *Q, const chain_tensor_t *K,
+                     const chain_tensor_t *V, const int32_t *cu_seqlens, int batch,
+                     int max_seqlen, int mask, float scale, chain_tensor_t *O,
+                     chain_tensor_t *LSE, void *stream);
+
+/*
  * sp_relayout -- Ulysses sequence shards -> head-major for one head group
  * ("Ulysses Sequence Parallelism", "Contexte Technique": every position of
  * the sequence, a subset of the heads).
@@ -248,7 +274,9 @@ int sp_relayout_inverse(const chain_tensor_t *in, int p, int head_group,
 /*
  * chain_check -- synchronise `stream`, then read and clear the device
  * status word.  Returns CHAIN_ERR_TIMEOUT if a bounded wait expired in any
- * kernel since the last check, CHAIN_ERR_CUDA on a CUDA error, else 0.
+ * kernel since the last check, CHAIN_ERR_ARG if a kernel met an argument only
+ * it could check (chain_fwd_varlen: a sequence longer than max_seqlen),
+ * CHAIN_ERR_CUDA on a CUDA error, else 0.
  * `detail` (may be NULL) receives the code of the wait site that expired.
  */
 int chain_check(void *stream, int *detail);

@@ -1,0 +1,96 @@
+"""GPU: attention over sequences of different lengths packed end to end
+(chain_fwd_varlen), against chain_fwd on each sequence alone (bit for bit)
+and the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import chain_synth as cs
+from tol import assert_fwd_close, assert_lse_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cg():
+    import chain_gb300
+    chain_gb300.lib()
+    return chain_gb300
+
+
+LENS = [300, 1, 129, 512, 77, 256]
+
+
+def _packed(lens, H, Hkv, d, seed):
+    total = sum(lens)
+    q = cs.normal((total, H, d), seed)
+    k = cs.normal((total, Hkv, d), seed + 1)
+    v = cs.normal((total, Hkv, d), seed + 2)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    return q, k, v, cu
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H,Hkv,d", [(4, 4, 128), (4, 2, 64), (6, 3, 128)])
+def test_varlen_matches_each_sequence_alone(cg, H, Hkv, d, causal):
+    q, k, v, cu = _packed(LENS, H, Hkv, d, seed=8400 + H + d)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = cg.attention_fwd_varlen(qd, kd, vd, cu.cuda(), max(LENS), causal)
+    assert cg.chain_check()[0] == 0
+    for b, L in enumerate(LENS):
+        lo, hi = int(cu[b]), int(cu[b + 1])
+        # the same sequence alone, head-major [H][L][d]
+        oa, la = cg.attention_fwd(qd[lo:hi].transpose(0, 1).contiguous(),
+                                  kd[lo:hi].transpose(0, 1).contiguous(),
+                                  vd[lo:hi].transpose(0, 1).contiguous(), causal)
+        assert torch.equal(o[lo:hi].transpose(0, 1).contiguous().view(torch.int16),
+                           oa.view(torch.int16)), f"O of sequence {b}"
+        assert torch.equal(lse[:, lo:hi].contiguous().view(torch.int32),
+                           la.view(torch.int32)), f"LSE of sequence {b}"
+
+
+def test_varlen_vs_oracle(cg, orc):
+    H, Hkv, d = 4, 2, 128
+    q, k, v, cu = _packed(LENS, H, Hkv, d, seed=8500)
+    o, lse = cg.attention_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cu.cuda(), max(LENS), True)
+    assert cg.chain_check()[0] == 0
+    G = H // Hkv
+    for b in range(len(LENS)):
+        lo, hi = int(cu[b]), int(cu[b + 1])
+        qs = q[lo:hi].transpose(0, 1).contiguous()
+        ks = k[lo:hi].transpose(0, 1).repeat_interleave(G, 0).contiguous()
+        vs = v[lo:hi].transpose(0, 1).repeat_interleave(G, 0).contiguous()
+        ro, rl = orc.softmax_fwd(qs, ks, vs, d ** -0.5, True)
+        assert_fwd_close(o.cpu()[lo:hi].transpose(0, 1), ro, f"varlen O seq {b}")
+        assert_lse_close(lse.cpu()[:, lo:hi], rl, f"varlen LSE seq {b}")
+
+
+def test_varlen_sequence_longer_than_max_is_reported(cg):
+    q, k, v, cu = _packed([300, 40], 2, 2, 128, seed=8600)
+    cg.attention_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cu.cuda(), 256, True)
+    rc, _ = cg.chain_check()
+    assert rc == cg.ERR_ARG
+    assert cg.chain_check()[0] == 0  # the report is cleared
+
+
+def test_varlen_offsets_clamped_to_the_tensor(cg):
+    # offsets past the packed rows are clamped on the device: no access
+    # outside the tensors, and the in-range sequence is still right
+    q, k, v, _ = _packed([128, 128], 2, 2, 128, seed=8700)
+    cu = torch.tensor([0, 128, 999], dtype=torch.int32, device="cuda")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, _ = cg.attention_fwd_varlen(qd, kd, vd, cu, 256, False)
+    assert cg.chain_check()[0] == 0
+    oa, _ = cg.attention_fwd(qd[:128].transpose(0, 1).contiguous(), kd[:128].transpose(0, 1).contiguous(),
+                             vd[:128].transpose(0, 1).contiguous(), False)
+    assert torch.equal(o[:128].transpose(0, 1).contiguous().view(torch.int16), oa.view(torch.int16))
+
+
+def test_varlen_rejects_bad_args(cg):
+    q = torch.zeros(64, 2, 128, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 64], dtype=torch.int32, device="cuda")
+    with pytest.raises(cg.ChainError):
+        cg.attention_fwd_varlen(q, q, q, cu, 65, True)       # max_seqlen > total
+    k = torch.zeros(64, 3, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(cg.ChainError):
+        cg.attention_fwd_varlen(q, k, k, cu, 64, True)        # 2 % 3 != 0
