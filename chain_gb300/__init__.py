@@ -74,6 +74,8 @@ def _load():
             lib.chain_bwd_workspace_size_f.restype = ctypes.c_size_t
             lib.chain_fwd_sp.argtypes = [P, P, P, ci, ci, ci, fl, P, P, vp]
             lib.chain_fwd_varlen.argtypes = [P, P, P, vp, ci, ci, ci, fl, P, P, vp]
+            lib.chain_bwd_varlen.argtypes = [P, P, P, P, P, P, vp, ci, ci, ci, fl, P, P, P, vp,
+                                             ctypes.c_size_t, vp]
             lib.sp_relayout.argtypes = [P, ci, ci, P, vp]
             lib.sp_relayout_inverse.argtypes = [P, ci, ci, P, vp]
             lib.chain_check.argtypes = [vp, ctypes.POINTER(ci)]
@@ -85,7 +87,8 @@ def _load():
             lib.chain_umma_selftest.argtypes = [vp, vp, vp, ci, ci, ci, vp]
             lib.chain_status_string.argtypes = [ci]
             lib.chain_status_string.restype = ctypes.c_char_p
-            for fn in ("chain_fwd", "chain_fwd_sp", "chain_fwd_varlen", "chain_bwd", "chain_bwd_noalloc",
+            for fn in ("chain_fwd", "chain_fwd_sp", "chain_fwd_varlen", "chain_bwd", "chain_bwd_varlen",
+                       "chain_bwd_noalloc",
                        "sp_relayout",
                        "sp_relayout_inverse",
                        "chain_check", "chain_selftest_wait_timeout", "chain_umma_selftest",
@@ -168,6 +171,19 @@ def chain_fwd_varlen(Q, K, V, cu_seqlens, batch, max_seqlen, mask, scale, O, LSE
                                  ctypes.c_void_p(cu_seqlens.data_ptr()), int(batch), int(max_seqlen),
                                  int(mask), float(scale), _ref(desc(O)), _ref(desc(LSE)),
                                  _stream(stream)), "chain_fwd_varlen")
+
+
+def chain_bwd_varlen(dO, Q, K, V, O, LSE, cu_seqlens, batch, max_seqlen, mask, scale, dQ, dK, dV,
+                     workspace, stream=None):
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+        raise ValueError("cu_seqlens must be a CUDA int32 tensor")
+    _ok(_load().chain_bwd_varlen(_ref(desc(dO)), _ref(desc(Q)), _ref(desc(K)), _ref(desc(V)),
+                                 _ref(desc(O)), _ref(desc(LSE)), ctypes.c_void_p(cu_seqlens.data_ptr()),
+                                 int(batch), int(max_seqlen), int(mask), float(scale),
+                                 _ref(desc(dQ)), _ref(desc(dK)), _ref(desc(dV)),
+                                 ctypes.c_void_p(workspace.data_ptr()),
+                                 ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                                 _stream(stream)), "chain_bwd_varlen")
 
 
 def chain_bwd_workspace_size(A, C) -> int:
@@ -274,6 +290,17 @@ def attention_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool,
     chain_fwd_varlen(q, k, v, cu_seqlens, cu_seqlens.numel() - 1, max_seqlen,
                      MASK_CAUSAL if causal else MASK_NONE, scale, o, lse, stream)
     return o, lse
+
+
+def attention_bwd_varlen(do, q, k, v, o, lse, cu_seqlens, max_seqlen: int, causal: bool,
+                         scale: float | None = None, stream=None):
+    """Gradients of attention_fwd_varlen: returns (dQ, dK, dV), packed like q, k, v."""
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    ws = torch.empty(chain_bwd_workspace_size(q, q), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    chain_bwd_varlen(do, q, k, v, o, lse, cu_seqlens, cu_seqlens.numel() - 1, max_seqlen,
+                     MASK_CAUSAL if causal else MASK_NONE, scale, dq, dk, dv, ws, stream)
+    return dq, dk, dv
 
 
 def attention_bwd(do, q, k, v, o, lse, causal: bool, scale: float | None = None,

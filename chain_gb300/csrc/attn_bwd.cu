@@ -72,10 +72,18 @@ struct BwdLayout {
 struct BwdParams {
   int BH, n, nb, causal;
   int G;  // query heads per K/V head (grouped-query attention; 1 = none)
+  // element strides: Q, O, dO, dQ rows / heads; K, V, dK, dV rows / heads;
+  // LSE and D heads (their rows are contiguous)
+  int64_t q_srow, q_shead, kv_srow, kv_shead, l_shead;
+  // Variable-length batch (null cu when not): sequence b is rows
+  // [cu[b], cu[b+1]) of the packed tensors; nb counts the blocks of the
+  // longest sequence.
+  const int *cu;
+  int nbatch;
   float scale, scale_log2;
   const float *LSE;   // [BH][n]
   const float *Dvec;  // [BH][n]
-  const __nv_bfloat16 *Q, *dO;  // [BH][n][D]
+  const __nv_bfloat16 *Q, *dO;
   __nv_bfloat16 *dQ, *dK, *dV;
   WaitCfg wc;
 };
@@ -126,21 +134,35 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16 *ro
   }
 }
 
+// One sequence of a variable-length batch: bounds clamped to the packed rows
+// so a bad cu can never address memory outside the tensors.
+__device__ __forceinline__ void seq_bounds(const BwdParams &p, int b, int &row0, int &n) {
+  int lo = __ldg(p.cu + b), hi = __ldg(p.cu + b + 1);
+  lo = lo < 0 ? 0 : (lo > p.n ? p.n : lo);
+  hi = hi < lo ? lo : (hi > p.n ? p.n : hi);
+  row0 = lo;
+  n = hi - lo;
+}
+
 // ------------------------------------------------------------ preprocess
 // 16 threads per row of d = 128 (8 per row of d = 64): each loads 16 bytes
 // of O and dO; the partial dot products are reduced with shuffles.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__restrict__ O,
                                                        const __nv_bfloat16 *__restrict__ dO,
-                                                       float *__restrict__ Dvec, int64_t rows) {
+                                                       float *__restrict__ Dvec, int64_t rows,
+                                                       int n, int64_t srow, int64_t shead,
+                                                       int64_t l_shead) {
   constexpr int TPR = D / 8;  // threads per row
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t row = tid / TPR;
+  const int64_t row = tid / TPR;  // head row / n, position row % n
   const int part = (int)(tid % TPR);
+  const int64_t h = row / n, t = row % n;
+  const int64_t off = h * shead + t * srow + part * 8;
   float acc = 0.0f;
   if (row < rows) {
-    const uint4 a = *reinterpret_cast<const uint4 *>(O + row * D + part * 8);
-    const uint4 b = *reinterpret_cast<const uint4 *>(dO + row * D + part * 8);
+    const uint4 a = *reinterpret_cast<const uint4 *>(O + off);
+    const uint4 b = *reinterpret_cast<const uint4 *>(dO + off);
     const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
     const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
 #pragma unroll
@@ -153,11 +175,11 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
   }
 #pragma unroll
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && part == 0) Dvec[row] = acc;
+  if (row < rows && part == 0) Dvec[h * l_shead + t] = acc;
 }
 
 // ------------------------------------------------------- dK, dV kernel
-template <int D>
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(NTHREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
@@ -191,10 +213,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // Tile t covers query tile i_begin + t % Tq of query head bkv*G + t / Tq
   // (Tq = nb - i_begin):
   // with grouped-query attention dK and dV sum over the group's heads.
-  const int bkv = blockIdx.x / p.nb;
-  const int jb = blockIdx.x % p.nb;
+  int bkv, jb, n = p.n, nb = p.nb, row0 = 0;
+  if constexpr (!VARLEN) {
+    bkv = blockIdx.x / p.nb;
+    jb = blockIdx.x % p.nb;
+  } else {
+    const int per_head = p.nbatch * p.nb;
+    bkv = blockIdx.x / per_head;
+    jb = blockIdx.x % p.nb;
+    seq_bounds(p, (blockIdx.x % per_head) / p.nb, row0, n);
+    nb = (n + BM - 1) / BM;
+    if (jb >= nb) return;  // nothing of this sequence for this CTA
+  }
   const int i_begin = p.causal ? jb : 0;
-  const int T = (p.nb - i_begin) * p.G;
+  const int T = (nb - i_begin) * p.G;
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 16; ++b)
@@ -225,11 +257,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_arrive_expect_tx(kv_full, 2 * L::T_BYTES);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(smem + L::A_K + c * (BM * 128), &tmK, kv_full, c * 64, jb * BM, bkv);
-        tma_load_3d(smem + L::A_V + c * (BM * 128), &tmV, kv_full, c * 64, jb * BM, bkv);
+        tma_load_3d(smem + L::A_K + c * (BM * 128), &tmK, kv_full, c * 64, row0 + jb * BM, bkv);
+        tma_load_3d(smem + L::A_V + c * (BM * 128), &tmV, kv_full, c * 64, row0 + jb * BM, bkv);
       }
       int i = i_begin, bh = bkv * p.G;  // query tile and head of tile t
-      for (int t = 0; t < T; ++t, (++i == p.nb) ? (i = i_begin, ++bh) : 0) {
+      for (int t = 0; t < T; ++t, (++i == nb) ? (i = i_begin, ++bh) : 0) {
         const int s = t & 1;
         if (t >= 2 && !mbar_wait(&q_empty[s], ((t >> 1) - 1) & 1, p.wc, abort_flag, SITE_BWD_PROD))
           break;
@@ -237,7 +269,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(smem + L::A_Q + s * L::T_BYTES + c * (BM * 128), &tmQ, &q_full[s], c * 64,
-                      i * BM, bh);
+                      row0 + i * BM, bh);
         q_issued = t + 1;
         if (t >= 2 && !mbar_wait(&do_empty[s], ((t >> 1) - 1) & 1, p.wc, abort_flag, SITE_BWD_PROD))
           break;
@@ -245,7 +277,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(smem + L::A_DO + s * L::T_BYTES + c * (BM * 128), &tmdO, &do_full[s], c * 64,
-                      i * BM, bh);
+                      row0 + i * BM, bh);
         do_issued = t + 1;
       }
       if (*abort_flag) {
@@ -368,7 +400,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int kv_idx = jb * BM + r;
-    const bool kv_ok = kv_idx < p.n;
+    const bool kv_ok = kv_idx < n;
     // P^T row r, queries [64w, 64w+64): 128 bytes of a 128B-swizzled tile
     const uint32_t pt_row = smem_u32(smem + L::A_PT + w * (BM * 128) + r * 128);
     float *wl = sL + w * 64;
@@ -377,15 +409,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // one tile ahead
     auto fetch = [&](int i, int bh, float &lv, float &dv) {
       const int q = i * BM + 64 * w + r;
-      const bool q_ok = r < 64 && q < p.n;
-      lv = q_ok ? __ldg(p.LSE + (int64_t)bh * p.n + q) * 1.4426950408889634f : INFINITY;
-      dv = q_ok ? __ldg(p.Dvec + (int64_t)bh * p.n + q) : 0.0f;
+      const bool q_ok = r < 64 && q < n;
+      const int64_t li = (int64_t)bh * p.l_shead + row0 + q;
+      lv = q_ok ? __ldg(p.LSE + li) * 1.4426950408889634f : INFINITY;
+      dv = q_ok ? __ldg(p.Dvec + li) : 0.0f;
     };
     float l_next = INFINITY, d_next = 0.0f;
     if (T > 0) fetch(i_begin, bkv * p.G, l_next, d_next);
     bool ok = true;
     int i = i_begin, bh = bkv * p.G;  // query tile and head of tile t
-    for (int t = 0; t < T; ++t, (++i == p.nb) ? (i = i_begin, ++bh) : 0) {
+    for (int t = 0; t < T; ++t, (++i == nb) ? (i = i_begin, ++bh) : 0) {
       const bool diag = p.causal && (i == jb);
       if (t > 0) named_bar_sync(1 + w, 128);  // warpgroup done with the staged values of t-1
       if (r < 64) {
@@ -394,7 +427,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       named_bar_sync(1 + w, 128);
       if (t + 1 < T) {
-        const bool wrap = i + 1 == p.nb;
+        const bool wrap = i + 1 == nb;
         fetch(wrap ? i_begin : i + 1, wrap ? bh + 1 : bh, l_next, d_next);
       }
       if (ok) ok = mbar_wait(s_full, t & 1, p.wc, abort_flag, SITE_BWD_COMPUTE);
@@ -466,7 +499,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok && T > 0 && mbar_wait(fin, 0, p.wc, abort_flag, SITE_BWD_EPI)) {
       tc_fence_after();
       // warpgroup 0 writes dV, warpgroup 1 writes dK (times scale)
-      __nv_bfloat16 *row = (w ? p.dK : p.dV) + ((int64_t)bkv * p.n + kv_idx) * D;
+      __nv_bfloat16 *row =
+          (w ? p.dK : p.dV) + (int64_t)bkv * p.kv_shead + (int64_t)(row0 + kv_idx) * p.kv_srow;
       store_row_bf16<D>((w ? tdK : tdV) + lane_off, row, w ? p.scale : 1.0f, kv_ok);
     }
   }
@@ -483,7 +517,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // Q_i and dO_i are the same for every key tile of a CTA, so they sit in
 // tensor memory as the A operand of S = Q_i K_j^T and dP = dO_i V_j^T: those
 // products then read only K_j or V_j from shared memory.
-template <int D>
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(NTHREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const BwdParams p) {
@@ -508,9 +542,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // head-major, heaviest (last) causal query tile first within a head
-  const int bh = blockIdx.x / p.nb;
-  const int ib = p.causal ? (p.nb - 1 - (int)(blockIdx.x % p.nb)) : (int)(blockIdx.x % p.nb);
-  const int NJ = p.causal ? ib + 1 : p.nb;
+  int bh, ib, n = p.n, nb = p.nb, row0 = 0;
+  if constexpr (!VARLEN) {
+    bh = blockIdx.x / p.nb;
+    ib = p.causal ? (p.nb - 1 - (int)(blockIdx.x % p.nb)) : (int)(blockIdx.x % p.nb);
+  } else {
+    const int per_head = p.nbatch * p.nb;
+    bh = blockIdx.x / per_head;
+    const int k = blockIdx.x % p.nb;
+    seq_bounds(p, (blockIdx.x % per_head) / p.nb, row0, n);
+    nb = (n + BM - 1) / BM;
+    if (k >= nb) return;  // nothing of this sequence for this CTA
+    ib = p.causal ? nb - 1 - k : k;
+  }
+  const int NJ = p.causal ? ib + 1 : nb;
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 19; ++b) {
@@ -550,7 +595,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(smem + L::B_K + sk * L::T_BYTES + c * (BM * 128), &tmK, &k_full[sk], c * 64,
-                      j * BM, bkv);
+                      row0 + j * BM, bkv);
         k_issued = j + 1;
         if (j >= 3 && !mbar_wait(&v_empty[sk], ((j / 3) - 1) & 1, p.wc, abort_flag, SITE_DQ_PROD))
           break;
@@ -558,7 +603,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(smem + L::B_V + sk * L::T_BYTES + c * (BM * 128), &tmV, &v_full[sk], c * 64,
-                      j * BM, bkv);
+                      row0 + j * BM, bkv);
         v_issued = j + 1;
       }
       if (*abort_flag) {
@@ -670,15 +715,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int q_idx = ib * BM + r;
-    const bool q_ok = q_idx < p.n;
-    const float lse2 = q_ok ? p.LSE[(int64_t)bh * p.n + q_idx] * 1.4426950408889634f : INFINITY;
-    const float dval = q_ok ? p.Dvec[(int64_t)bh * p.n + q_idx] : 0.0f;
+    const bool q_ok = q_idx < n;
+    const int64_t li = (int64_t)bh * p.l_shead + row0 + q_idx;
+    const float lse2 = q_ok ? p.LSE[li] * 1.4426950408889634f : INFINITY;
+    const float dval = q_ok ? p.Dvec[li] : 0.0f;
     // warpgroup 0 puts row q_idx of Q into tensor memory, warpgroup 1 the
     // same row of dO (zeros past n); the bf16 pairs of a row are already
     // the packed column words
     {
       const uint4 *src = reinterpret_cast<const uint4 *>((w ? p.dO : p.Q) +
-                                                         ((int64_t)bh * p.n + q_idx) * D);
+                                                         (int64_t)bh * p.q_shead +
+                                                         (int64_t)(row0 + q_idx) * p.q_srow);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         uint32_t v[32];
@@ -698,7 +745,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     bool ok = true;
     for (int j = 0; j < NJ; ++j) {
-      const bool masked = (p.causal && j == ib) || ((j + 1) * BM > p.n);
+      const bool masked = (p.causal && j == ib) || ((j + 1) * BM > n);
       if (!mbar_wait(s_full, j & 1, p.wc, abort_flag, SITE_DQ_COMPUTE)) {
         ok = false;
         break;
@@ -720,7 +767,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
             const int kv = j * BM + 64 * w + c;
-            if ((p.causal && kv > q_idx) || kv >= p.n) pf[c] = 0.0f;
+            if ((p.causal && kv > q_idx) || kv >= n) pf[c] = 0.0f;
           }
         }
       }
@@ -750,7 +797,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok && mbar_wait(fin, 0, p.wc, abort_flag, SITE_DQ_EPI)) {
       tc_fence_after();
       // warpgroup w writes columns [w D/2, (w+1) D/2) of dQ row q_idx
-      __nv_bfloat16 *row = p.dQ + ((int64_t)bh * p.n + q_idx) * D + w * (D / 2);
+      __nv_bfloat16 *row =
+          p.dQ + (int64_t)bh * p.q_shead + (int64_t)(row0 + q_idx) * p.q_srow + w * (D / 2);
       store_row_bf16<D / 2>(tdQ + lane_off + w * (D / 2), row, p.scale, q_ok);
     }
   }
@@ -766,31 +814,40 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 template <int D>
 cudaError_t launch_bwd_d(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t st) {
   using L = BwdLayout<D>;
-  const int64_t rows = (int64_t)a.BH * a.n;
   cudaError_t e;
   {
+    const int64_t rows = (int64_t)a.BH * a.n;  // every (head, position)
     const int64_t threads = rows * (D / 8);
     const unsigned grid = (unsigned)((threads + 255) / 256);
     bwd_prep_kernel<D><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(a.O),
                                              static_cast<const __nv_bfloat16 *>(a.dO), a.Dvec,
-                                             rows);
+                                             rows, a.n, a.q_srow, a.q_shead, a.l_shead);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   CUtensorMap mq, mk, mv, mdo;
   const uint32_t box[3] = {64, 128, 1};
   const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.n, (uint64_t)a.BH};
   const uint64_t dkv[3] = {(uint64_t)D, (uint64_t)a.n, (uint64_t)a.BHkv};
-  const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)a.n * D * 2};
-  if ((e = make_tmap(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.Q, dims, str, box))) return e;
-  if ((e = make_tmap(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.K, dkv, str, box))) return e;
-  if ((e = make_tmap(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.V, dkv, str, box))) return e;
-  if ((e = make_tmap(&mdo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.dO, dims, str, box))) return e;
+  const uint64_t sq[2] = {(uint64_t)a.q_srow * 2, (uint64_t)a.q_shead * 2};
+  const uint64_t skv[2] = {(uint64_t)a.kv_srow * 2, (uint64_t)a.kv_shead * 2};
+  if ((e = make_tmap(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.Q, dims, sq, box))) return e;
+  if ((e = make_tmap(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.K, dkv, skv, box))) return e;
+  if ((e = make_tmap(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.V, dkv, skv, box))) return e;
+  if ((e = make_tmap(&mdo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.dO, dims, sq, box))) return e;
   BwdParams p;
   p.BH = a.BH;
   p.n = a.n;
-  p.nb = (a.n + BM - 1) / BM;
+  // with a variable-length batch, blocks per head come from the longest sequence
+  p.nb = ((a.cu_seqlens ? a.max_seqlen : a.n) + BM - 1) / BM;
   p.causal = a.causal;
   p.G = a.BH / a.BHkv;
+  p.q_srow = a.q_srow;
+  p.q_shead = a.q_shead;
+  p.kv_srow = a.kv_srow;
+  p.kv_shead = a.kv_shead;
+  p.l_shead = a.l_shead;
+  p.cu = a.cu_seqlens;
+  p.nbatch = a.nbatch;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.LSE = a.LSE;
@@ -801,13 +858,15 @@ cudaError_t launch_bwd_d(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t s
   p.dK = static_cast<__nv_bfloat16 *>(a.dK);
   p.dV = static_cast<__nv_bfloat16 *>(a.dV);
   p.wc = wc;
-  auto ka = bwd_dkdv_kernel<D>;
-  auto kb = bwd_dq_kernel<D>;
+  const bool varlen = a.cu_seqlens != nullptr;
+  auto ka = varlen ? bwd_dkdv_kernel<D, true> : bwd_dkdv_kernel<D, false>;
+  auto kb = varlen ? bwd_dq_kernel<D, true> : bwd_dq_kernel<D, false>;
   if ((e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, L::A_ALLOC)))
     return e;
   if ((e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, L::B_ALLOC)))
     return e;
-  const unsigned grid_kv = (unsigned)(p.nb * a.BHkv), grid_q = (unsigned)(p.nb * a.BH);
+  const unsigned nseq = varlen ? (unsigned)a.nbatch : 1u;
+  const unsigned grid_kv = (unsigned)(p.nb * a.BHkv) * nseq, grid_q = (unsigned)(p.nb * a.BH) * nseq;
   timing_mark(st, 0);
   ka<<<grid_kv, NTHREADS, L::A_ALLOC, st>>>(mq, mk, mv, mdo, p);
   timing_mark(st, 1);

@@ -458,6 +458,10 @@ int chain_bwd(const chain_tensor_t *dO, const chain_tensor_t *A, const chain_ten
   args.BH = (int)q.outer; args.n = (int)q.rows; args.d = (int)q.cols;
   args.BHkv = (int)k.outer;
   args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
+  args.q_srow = args.kv_srow = q.cols;
+  args.q_shead = args.kv_shead = q.rows * q.cols;
+  args.l_shead = q.rows;
+  args.cu_seqlens = nullptr; args.nbatch = 0; args.max_seqlen = 0;
   DevInfo *di = nullptr;
   if ((rc = device_ready(&di))) return rc;
   cudaError_t e = launch_attn_bwd(args, wait_cfg(di), static_cast<cudaStream_t>(stream));
@@ -590,6 +594,49 @@ int chain_fwd_varlen(const chain_tensor_t *Q, const chain_tensor_t *K, const cha
   DevInfo *di = nullptr;
   if ((rc = device_ready(&di))) return rc;
   cudaError_t e = launch_attn_fwd_bf16(args, wait_cfg(di), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
+}
+
+int chain_bwd_varlen(const chain_tensor_t *dO, const chain_tensor_t *Q, const chain_tensor_t *K,
+                     const chain_tensor_t *V, const chain_tensor_t *O, const chain_tensor_t *LSE,
+                     const int32_t *cu_seqlens, int batch, int max_seqlen, int mask, float scale,
+                     chain_tensor_t *dQ, chain_tensor_t *dK, chain_tensor_t *dV, void *workspace,
+                     size_t ws_bytes, void *stream) {
+  if (!Q || Q->ndim != 3 || !K || K->ndim != 3) return CHAIN_ERR_ARG;
+  if (mask != CHAIN_MASK_NONE && mask != CHAIN_MASK_CAUSAL) return CHAIN_ERR_ARG;
+  const int64_t total = Q->shape[0], H = Q->shape[1], d = Q->shape[2], Hkv = K->shape[1];
+  const chain_tensor_t *qs[4] = {Q, O, dO, dQ}, *ks[4] = {K, V, dK, dV};
+  int rc;
+  for (int i = 0; i < 4; ++i) {
+    if ((rc = packed_view(qs[i], total, H, d)) || (rc = packed_view(ks[i], total, Hkv, d))) return rc;
+    // one stride pair serves each side
+    if (qs[i]->stride[0] != Q->stride[0] || qs[i]->stride[1] != Q->stride[1]) return CHAIN_ERR_ARG;
+    if (ks[i]->stride[0] != K->stride[0] || ks[i]->stride[1] != K->stride[1]) return CHAIN_ERR_ARG;
+  }
+  if (total < 1 || total > (1 << 30) || (d != 64 && d != 128)) return CHAIN_ERR_ARG;
+  if (Hkv < 1 || H % Hkv || H > 65535 * 16) return CHAIN_ERR_ARG;
+  if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return CHAIN_ERR_ARG;
+  if (batch < 1 || batch > (1 << 20) || max_seqlen < 1 || max_seqlen > total) return CHAIN_ERR_ARG;
+  if (!(scale > 0.0f) || !(scale < 1e30f)) return CHAIN_ERR_ARG;
+  int64_t lse_sbh = 0;
+  if ((rc = lse_view(LSE, H, total, &lse_sbh))) return rc;
+  if (lse_sbh != total) return CHAIN_ERR_ARG;
+  const size_t need = ((size_t)H * (size_t)total * sizeof(float) + 255) & ~size_t(255);
+  if (!workspace || ws_bytes < need || !aligned16(workspace)) return CHAIN_ERR_ARG;
+  AttnBwdArgs args;
+  args.Q = Q->ptr; args.K = K->ptr; args.V = V->ptr; args.O = O->ptr; args.dO = dO->ptr;
+  args.LSE = static_cast<const float *>(LSE->ptr);
+  args.dQ = dQ->ptr; args.dK = dK->ptr; args.dV = dV->ptr;
+  args.Dvec = static_cast<float *>(workspace);
+  args.BH = (int)H; args.BHkv = (int)Hkv; args.n = (int)total; args.d = (int)d;
+  args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
+  args.q_srow = Q->stride[0]; args.q_shead = Q->stride[1];
+  args.kv_srow = K->stride[0]; args.kv_shead = K->stride[1];
+  args.l_shead = total;
+  args.cu_seqlens = cu_seqlens; args.nbatch = batch; args.max_seqlen = max_seqlen;
+  DevInfo *di = nullptr;
+  if ((rc = device_ready(&di))) return rc;
+  cudaError_t e = launch_attn_bwd(args, wait_cfg(di), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
 }
 

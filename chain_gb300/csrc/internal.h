@@ -46,6 +46,13 @@ struct AttnBwdArgs {
   int BH, n, d, causal;
   int BHkv;  // K/V heads (grouped-query attention: BH / BHkv query heads each)
   float scale;
+  // element strides: Q, O, dO, dQ (row, head); K, V, dK, dV (row, head);
+  // LSE and D head stride (rows contiguous)
+  int64_t q_srow, q_shead, kv_srow, kv_shead, l_shead;
+  // Variable-length batch: device int32 [nbatch + 1] row offsets into the
+  // packed rows (n = total rows), or null.
+  const int *cu_seqlens;
+  int nbatch, max_seqlen;
 };
 cudaError_t launch_attn_bwd(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t st);
 

@@ -251,6 +251,25 @@ int chain_fwd_varlen(const chain_tensor_t *Q, const chain_tensor_t *K,
                      chain_tensor_t *LSE, void *stream);
 
 /*
+ * chain_bwd_varlen -- gradients of chain_fwd_varlen (softmax attention over
+ * sequences packed end to end), S and P recomputed from LSE as in chain_bwd.
+ *   dO, Q, O, dQ  [total][H][d] bf16, one set of strides for the four;
+ *   K, V, dK, dV  [total][Hkv][d] bf16, one set of strides for the four
+ *                 (grouped-query attention: dK, dV sum over each group);
+ *   LSE           [H][total] fp32 as written by chain_fwd_varlen (dense);
+ *   cu_seqlens, batch, max_seqlen, mask, scale as for chain_fwd_varlen.
+ *   workspace     at least 4 * H * total bytes rounded up to 256, 16-byte
+ *                 aligned (chain_bwd_workspace_size(Q, Q) returns it).
+ * Each sequence's gradients are those chain_bwd gives for it alone.
+ */
+int chain_bwd_varlen(const chain_tensor_t *dO, const chain_tensor_t *Q,
+                     const chain_tensor_t *K, const chain_tensor_t *V,
+                     const chain_tensor_t *O, const chain_tensor_t *LSE,
+                     const int32_t *cu_seqlens, int batch, int max_seqlen, int mask,
+                     float scale, chain_tensor_t *dQ, chain_tensor_t *dK,
+                     chain_tensor_t *dV, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * sp_relayout -- Ulysses sequence shards -> head-major for one head group
  * ("Ulysses Sequence Parallelism", "Contexte Technique": every position of
  * the sequence, a subset of the heads).

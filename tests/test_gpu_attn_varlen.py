@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import chain_synth as cs
-from tol import assert_fwd_close, assert_lse_close
+from tol import assert_fwd_close, assert_grad_close, assert_lse_close
 
 pytestmark = pytest.mark.gpu
 
@@ -94,3 +94,46 @@ def test_varlen_rejects_bad_args(cg):
     k = torch.zeros(64, 3, 128, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(cg.ChainError):
         cg.attention_fwd_varlen(q, k, k, cu, 64, True)        # 2 % 3 != 0
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H,Hkv,d", [(4, 4, 128), (4, 2, 64)])
+def test_varlen_bwd_matches_each_sequence_alone(cg, H, Hkv, d, causal):
+    q, k, v, cu = _packed(LENS, H, Hkv, d, seed=8800 + H + d)
+    do = cs.normal(tuple(q.shape), 8899)
+    qd, kd, vd, dod, cud = q.cuda(), k.cuda(), v.cuda(), do.cuda(), cu.cuda()
+    o, lse = cg.attention_fwd_varlen(qd, kd, vd, cud, max(LENS), causal)
+    dq, dk, dv = cg.attention_bwd_varlen(dod, qd, kd, vd, o, lse, cud, max(LENS), causal)
+    assert cg.chain_check()[0] == 0
+    hm = lambda x, lo, hi: x[lo:hi].transpose(0, 1).contiguous()
+    for b, L in enumerate(LENS):
+        lo, hi = int(cu[b]), int(cu[b + 1])
+        oa, la = cg.attention_fwd(hm(qd, lo, hi), hm(kd, lo, hi), hm(vd, lo, hi), causal)
+        ga = cg.attention_bwd(hm(dod, lo, hi), hm(qd, lo, hi), hm(kd, lo, hi), hm(vd, lo, hi), oa, la,
+                              causal)
+        for name, got, ref in (("dQ", dq, ga[0]), ("dK", dk, ga[1]), ("dV", dv, ga[2])):
+            assert torch.equal(hm(got, lo, hi).view(torch.int16), ref.view(torch.int16)), \
+                f"{name} of sequence {b}"
+
+
+def test_varlen_bwd_vs_oracle(cg, orc):
+    H, Hkv, d = 4, 2, 128
+    lens = [200, 64, 333]
+    q, k, v, cu = _packed(lens, H, Hkv, d, seed=8900)
+    do = cs.normal(tuple(q.shape), 8999)
+    o, lse = cg.attention_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cu.cuda(), max(lens), True)
+    dq, dk, dv = cg.attention_bwd_varlen(do.cuda(), q.cuda(), k.cuda(), v.cuda(), o, lse, cu.cuda(),
+                                         max(lens), True)
+    assert cg.chain_check()[0] == 0
+    G = H // Hkv
+    for b in range(len(lens)):
+        lo, hi = int(cu[b]), int(cu[b + 1])
+        hm = lambda x: x[lo:hi].transpose(0, 1).contiguous()
+        rq, rk, rv, _ = orc.softmax_bwd(hm(q), hm(k).repeat_interleave(G, 0), hm(v).repeat_interleave(G, 0),
+                                        hm(do), d ** -0.5, True)
+        n = hi - lo
+        rk = np.asarray(rk).reshape(Hkv, G, n, d).sum(1)
+        rv = np.asarray(rv).reshape(Hkv, G, n, d).sum(1)
+        assert_grad_close(hm(dq.cpu()), rq, f"varlen dQ seq {b}")
+        assert_grad_close(hm(dk.cpu()), rk, f"varlen dK seq {b}")
+        assert_grad_close(hm(dv.cpu()), rv, f"varlen dV seq {b}")
