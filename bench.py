@@ -513,6 +513,63 @@ def measure_mlp_bwd(hp, reps=10):
         "flops": fl, "timing": f"median of {reps}, L2 flushed between iterations"}}
 
 
+def measure_fp8(hp, reps=5):
+    """The causal 32 x 32768 x 128 forward on e4m3 Q, K, V (chain_fwd_fp8):
+    the V re-encoding kernel and the attention kernel, timed at their
+    boundaries.  Measured beside the step, not part of its value."""
+    torch, cg, cs = hp.torch, hp.cg, hp.cs
+    wl = cs.WORKLOADS["causal_attn_32k_e4m3"]
+    dm = wl.dims
+    BH, n, d = dm["BH"], dm["n"], dm["d"]
+    q, k, v = cs.attn_inputs(BH, n, d, seed=wl.seed, dtype=torch.float8_e4m3fn, device=hp.dev)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=hp.dev)
+    lse = torch.empty(BH, n, dtype=torch.float32, device=hp.dev)
+    ws = torch.empty(cg.chain_fwd_fp8_workspace_size(v), dtype=torch.uint8, device=hp.dev)
+
+    def run(evs=None):
+        if evs is not None:
+            cg.set_timing_events(*evs)
+        cg.chain_fwd_fp8(q, k, v, cg.MASK_CAUSAL, d ** -0.5, 1.0, o, lse, ws)
+        if evs is not None:
+            cg.set_timing_events()
+
+    for _ in range(2):
+        run()
+    tot, conv, attn = [], [], []
+    for _ in range(reps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        torch.cuda.synchronize()
+        run(evs)
+        torch.cuda.synchronize()
+        conv.append(evs[0].elapsed_time(evs[1]))
+        attn.append(evs[1].elapsed_time(evs[2]))
+        tot.append(evs[0].elapsed_time(evs[2]))
+    rc, site = cg.chain_check()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} site {site:#x} in the e4m3 measurement")
+    med = lambda x: sorted(x)[len(x) // 2]
+    fl = attn_fwd_flops(BH, n, d, True)
+    peaks, src = load_peaks()
+    p16 = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    # half the counted products (Q K^T) run at the 8-bit rate, nominally twice
+    # the 16-bit one; the other half (P V) at the 16-bit rate
+    peak = 4.0 / 3.0 * p16
+    ka = fl / (med(attn) * 1e-3) / 1e12
+    vbytes = 3.0 * BH * n * d  # e4m3 read, f16 written
+    del q, k, v, o, lse, ws
+    return {"attn_fwd_fp8_causal_32x32768x128": {
+        "ms": round(med(tot), 4), "TFLOPs": round(fl / (med(tot) * 1e-3) / 1e12, 1),
+        "attn_kernel_ms": round(med(attn), 4), "attn_kernel_TFLOPs": round(ka, 1),
+        "v_convert_ms": round(med(conv), 4),
+        "v_convert_GBps": round(vbytes / (med(conv) * 1e-3) / 1e9, 1),
+        "roofline": {"bound": "tensor", "kernel": "attn_fwd_fp8_kernel", "achieved": round(ka, 1),
+                     "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(ka / peak, 4),
+                     "peak_basis": f"4/3 x {src} sustained bf16 (Q K^T at the nominal 2x "
+                                   "8-bit rate, P V at the 16-bit rate)"},
+        "inputs": "e4m3 Q, K, V (fp32 N(0,1) draws rounded to e4m3), O bf16",
+        "timing": f"median of {reps} after 2 warm-ups; inputs larger than L2"}}
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -539,6 +596,16 @@ def main():
     peaks, peak_src = load_peaks()
     hp = HotPath(dev, only=args.only)
     stream = torch.cuda.current_stream()
+    if not hp.comp:
+        # --only matched no component of the step: the rows measured beside it
+        nxt = {}
+        if "fp8" in (args.only or ""):
+            nxt.update(measure_fp8(hp))
+        if rank == 0:
+            print(json.dumps({"only": args.only, "next_rows": nxt or None}))
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
 
     ncomp = len(hp.comp)
     for _ in range(args.warmup):
@@ -699,6 +766,8 @@ def main():
         nxt.update(measure_sp_fused(hp))
     if hp.mlp_ok:
         nxt.update(measure_mlp_bwd(hp))
+    if args.only is None or "fp8" in args.only:
+        nxt.update(measure_fp8(hp))
     nxt = nxt or None
 
     cpu = None

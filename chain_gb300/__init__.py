@@ -25,7 +25,7 @@ import torch
 
 F_IDENTITY, F_SOFTMAX, F_GELU_TANH = 0, 1, 2
 MASK_NONE, MASK_CAUSAL = 0, 1
-BF16, F32 = 0, 1
+BF16, F32, E4M3 = 0, 1, 2
 
 OK, ERR_ARG, ERR_DTYPE, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
 ERR_SCRATCH_LIMIT = -7
@@ -76,6 +76,9 @@ def _load():
             lib.chain_fwd_varlen.argtypes = [P, P, P, vp, ci, ci, ci, fl, P, P, vp]
             lib.chain_bwd_varlen.argtypes = [P, P, P, P, P, P, vp, ci, ci, ci, fl, P, P, P, vp,
                                              ctypes.c_size_t, vp]
+            lib.chain_fwd_fp8.argtypes = [P, P, P, ci, fl, fl, P, P, vp, ctypes.c_size_t, vp]
+            lib.chain_fwd_fp8_workspace_size.argtypes = [P]
+            lib.chain_fwd_fp8_workspace_size.restype = ctypes.c_size_t
             lib.sp_relayout.argtypes = [P, ci, ci, P, vp]
             lib.sp_relayout_inverse.argtypes = [P, ci, ci, P, vp]
             lib.chain_check.argtypes = [vp, ctypes.POINTER(ci)]
@@ -88,7 +91,7 @@ def _load():
             lib.chain_status_string.argtypes = [ci]
             lib.chain_status_string.restype = ctypes.c_char_p
             for fn in ("chain_fwd", "chain_fwd_sp", "chain_fwd_varlen", "chain_bwd", "chain_bwd_varlen",
-                       "chain_bwd_noalloc",
+                       "chain_bwd_noalloc", "chain_fwd_fp8",
                        "sp_relayout",
                        "sp_relayout_inverse",
                        "chain_check", "chain_selftest_wait_timeout", "chain_umma_selftest",
@@ -111,6 +114,10 @@ def _dt(t: torch.Tensor) -> int:
         return BF16  # 2-byte payload (relayout moves bits only)
     if t.dtype == torch.int32:
         return F32  # 4-byte payload
+    if t.dtype == torch.float8_e4m3fn:
+        return E4M3
+    if t.dtype == torch.uint8 or t.dtype == torch.int8:
+        return E4M3  # 1-byte payload (relayout moves bits only)
     raise TypeError(f"chain_gb300: unsupported dtype {t.dtype}")
 
 
@@ -152,6 +159,19 @@ def chain_fwd(A, B, C, f, mask, scale, O, LSE=None, stream=None):
     _ok(_load().chain_fwd(_ref(desc(A)), _ref(desc(B)), _ref(desc(C)), int(f), int(mask),
                           float(scale), _ref(desc(O)), _ref(desc(LSE)), _stream(stream)),
         "chain_fwd")
+
+
+def chain_fwd_fp8(Q, K, V, mask, scale, v_scale, O, LSE, workspace, stream=None):
+    """Attention on e4m3 Q, K, V (d = 128) into bf16 O; see include/chain.h."""
+    _ok(_load().chain_fwd_fp8(_ref(desc(Q)), _ref(desc(K)), _ref(desc(V)), int(mask), float(scale),
+                              float(v_scale), _ref(desc(O)), _ref(desc(LSE)),
+                              ctypes.c_void_p(workspace.data_ptr()),
+                              workspace.numel() * workspace.element_size(), _stream(stream)),
+        "chain_fwd_fp8")
+
+
+def chain_fwd_fp8_workspace_size(V) -> int:
+    return int(_load().chain_fwd_fp8_workspace_size(_ref(desc(V))))
 
 
 def chain_fwd_sp(Q, K, V, p, head_group, mask, scale, O, LSE, stream=None):
@@ -263,6 +283,20 @@ def attention_fwd(q, k, v, causal: bool, scale: float | None = None, stream=None
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     chain_fwd(q, k, v, F_SOFTMAX, MASK_CAUSAL if causal else MASK_NONE, scale, o, lse, stream)
+    return o, lse
+
+
+def attention_fwd_fp8(q, k, v, causal: bool, scale: float | None = None, v_scale: float = 1.0,
+                      workspace=None, stream=None):
+    """Returns (O bf16, LSE) for e4m3 q [BH, n, 128], k, v [BHkv, n, 128]."""
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(max(chain_fwd_fp8_workspace_size(v), 16), dtype=torch.uint8,
+                                device=q.device)
+    chain_fwd_fp8(q, k, v, MASK_CAUSAL if causal else MASK_NONE, scale, v_scale, o, lse, workspace,
+                  stream)
     return o, lse
 
 

@@ -30,6 +30,14 @@
 //              P_t(j+1) may overwrite P_t(j) as soon as S_t(j+1) is read.
 // Tensor memory: S_a/P_a [0,128), S_b/P_b [128,256), O_a [256,384),
 // O_b [384,512).
+//
+// 8-bit inputs (attn_fwd_fp8_kernel): Q and K in e4m3, S = Q K^T by the
+// kind::f8f6f4 tensor-core product (K = 32 per instruction, one 128-byte
+// swizzled row per d = 128 row).  P is written back as one f16 per key
+// (keys [32g, 32g+32) in columns [16g, 16g+16)): f16 keeps 11 significant
+// bits, so no compensating low part is needed.  V arrives as f16 holding
+// e4m3 value x 2^-8 (an exact re-encoding made by v_e4m3_to_f16_kernel) and
+// the epilogue multiplies by 2^8 times the caller's V scale.
 #include "internal.h"
 
 namespace chain {
@@ -41,14 +49,16 @@ constexpr int STAGES = 2;
 constexpr int NTHREADS = 320;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 
-template <int D>
+template <int D, bool FP8>
 struct FwdLayout {
-  static constexpr uint32_t Q_BYTES = BM * D * 2;
-  static constexpr uint32_t KV_BYTES = BN * D * 2;
+  static constexpr uint32_t QK_ELEM = FP8 ? 1 : 2;            // bytes per Q/K element
+  static constexpr uint32_t Q_BYTES = BM * D * QK_ELEM;
+  static constexpr uint32_t K_BYTES = BN * D * QK_ELEM;
+  static constexpr uint32_t V_BYTES = BN * D * 2;             // bf16 or f16
   static constexpr uint32_t OFF_Q = 0;                        // Q_a, Q_b
   static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_BYTES;      // STAGES
-  static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + STAGES * K_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + STAGES * V_BYTES;
   // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2],
   // p_ready[2], pv_done[2], mma_drain
   static constexpr uint32_t NBAR = 1 + 4 * STAGES + 2 + 2 + 2 + 1;
@@ -69,6 +79,7 @@ struct FwdParams {
   int nbatch;
   int n_loc;  // positions per sequence shard (n when unsharded)
   float scale_log2;
+  float o_scale;  // 8-bit inputs: 2^8 x the V scale, applied with 1/l
   __nv_bfloat16 *O;
   int64_t o_sbh, o_srow, o_sshard;
   float *LSE;
@@ -108,12 +119,13 @@ __device__ __forceinline__ int kv_tiles(const FwdParams &p, int nkb, int qb, int
   return last < nkb ? last : nkb;
 }
 
-template <int D, bool SHARDED, bool VARLEN>
-__global__ void __launch_bounds__(NTHREADS, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
-                    const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using L = FwdLayout<D>;
+template <int D, bool SHARDED, bool VARLEN, bool FP8>
+__device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                                              const CUtensorMap &tmV, const FwdParams &p) {
+  static_assert(!FP8 || (D == 128 && !SHARDED && !VARLEN), "8-bit inputs: dense d = 128 only");
+  using L = FwdLayout<D, FP8>;
+  // Q/K boxes: 128-byte rows of 64 bf16 or 128 e4m3 elements
+  constexpr int QK_BOX = 128 / L::QK_ELEM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -214,27 +226,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
       for (int t = 0; t < 2; ++t)
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          load(smem + L::OFF_Q + t * L::Q_BYTES + c * (BM * 128), &tmQ, q_full, c * 64,
+        for (int c = 0; c < D / QK_BOX; ++c)
+          load(smem + L::OFF_Q + t * L::Q_BYTES + c * (BM * 128), &tmQ, q_full, c * QK_BOX,
                (2 * qb + t) * BM, bh);
       for (int j = 0; j < nkv_b; ++j) {
         const int st = j % STAGES;
         if (j >= STAGES &&
             !mbar_wait(&k_empty[st], ((j / STAGES) - 1) & 1, p.wc, abort_flag, SITE_FWD_PROD))
           break;
-        mbar_arrive_expect_tx(&k_full[st], L::KV_BYTES);
+        mbar_arrive_expect_tx(&k_full[st], L::K_BYTES);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          load(smem + L::OFF_K + st * L::KV_BYTES + c * (BN * 128), &tmK, &k_full[st], c * 64,
+        for (int c = 0; c < D / QK_BOX; ++c)
+          load(smem + L::OFF_K + st * L::K_BYTES + c * (BN * 128), &tmK, &k_full[st], c * QK_BOX,
                j * BN, bkv);
         k_issued = j + 1;
         if (j >= STAGES &&
             !mbar_wait(&v_empty[st], ((j / STAGES) - 1) & 1, p.wc, abort_flag, SITE_FWD_PROD))
           break;
-        mbar_arrive_expect_tx(&v_full[st], L::KV_BYTES);
+        mbar_arrive_expect_tx(&v_full[st], L::V_BYTES);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          load(smem + L::OFF_V + st * L::KV_BYTES + c * (BN * 128), &tmV, &v_full[st], c * 64,
+          load(smem + L::OFF_V + st * L::V_BYTES + c * (BN * 128), &tmV, &v_full[st], c * 64,
                j * BN, bkv);
         v_issued = j + 1;
       }
@@ -253,37 +265,49 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // The whole warp runs the loop; one elected lane issues each group of
     // products together with its commits.
     {
-      const uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
-      const uint32_t idO = idesc_bf16_f32(BM, D, 0, 1);
+      const uint32_t idS = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, 0, 0);
+      const uint32_t idO = FP8 ? idesc_f16_f32(BM, D, 0, 1) : idesc_bf16_f32(BM, D, 0, 1);
       // Base descriptors built once; every MMA below only adds a
       // compile-time byte offset to the low word.
       const SDesc dQ0 = sdesc_make(smem_u32(smem + L::OFF_Q), 16, 1024);
       const SDesc dQ1 = sdesc_make(smem_u32(smem + L::OFF_Q + L::Q_BYTES), 16, 1024);
       const SDesc dK0 = sdesc_make(smem_u32(smem + L::OFF_K), 16, 1024);
-      const SDesc dK1 = sdesc_make(smem_u32(smem + L::OFF_K + L::KV_BYTES), 16, 1024);
+      const SDesc dK1 = sdesc_make(smem_u32(smem + L::OFF_K + L::K_BYTES), 16, 1024);
       const SDesc dV0 = sdesc_make(smem_u32(smem + L::OFF_V), BN * 128, 1024);
-      const SDesc dV1 = sdesc_make(smem_u32(smem + L::OFF_V + L::KV_BYTES), BN * 128, 1024);
+      const SDesc dV1 = sdesc_make(smem_u32(smem + L::OFF_V + L::V_BYTES), BN * 128, 1024);
       static_assert(STAGES == 2, "descriptor selection assumes two stages");
-      // S_t(j) = Q_t K_j^T into columns [128t, 128t+128)
+      // S_t(j) = Q_t K_j^T into columns [128t, 128t+128); each product
+      // takes a 32-byte K slice of the 128-byte rows (16 bf16 or 32 e4m3)
       auto issue_s = [&](int t, int j) {
         const SDesc a = t ? dQ1 : dQ0;
         const SDesc b = (j & 1) ? dK1 : dK0;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D * (int)L::QK_ELEM / 32; ++kk) {
           const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          umma_f16_ss(tmem + t * BN, sdesc_at(a, off), sdesc_at(b, off), idS, kk > 0 ? 1u : 0u);
+          if constexpr (FP8)
+            umma_f8_ss(tmem + t * BN, sdesc_at(a, off), sdesc_at(b, off), idS, kk > 0 ? 1u : 0u);
+          else
+            umma_f16_ss(tmem + t * BN, sdesc_at(a, off), sdesc_at(b, off), idS, kk > 0 ? 1u : 0u);
         }
       };
-      // O_t += P_hi V_j + P_lo V_j, P read from tensor memory
+      // O_t += P_hi V_j + P_lo V_j (8-bit inputs: O_t += P V_j, one f16 P
+      // per key), P read from tensor memory
       auto issue_pv = [&](int t, int j) {
         const SDesc b = (j & 1) ? dV1 : dV0;
         const uint32_t tP = tmem + t * BN;
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
+        if constexpr (FP8) {
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            umma_f16_ts(tmem + 256 + t * 128, tP + kk * 16 + part * 8, sdesc_at(b, kk * 2048), idO,
-                        (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
+            umma_f16_ts(tmem + 256 + t * 128, tP + kk * 8, sdesc_at(b, kk * 2048), idO,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              umma_f16_ts(tmem + 256 + t * 128, tP + kk * 16 + part * 8, sdesc_at(b, kk * 2048),
+                          idO, (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
+        }
       };
       bool ok = mbar_wait_warp(q_full, 0, p.wc, abort_flag, SITE_FWD_MMA) &&
                 mbar_wait_warp(&k_full[0], 0, p.wc, abort_flag, SITE_FWD_MMA);
@@ -404,8 +428,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // over the columns already read: keys [16g, 16g+16) go to columns
       // [16g, 16g+8) (P_hi) and [16g+8, 16g+16) (P_lo), two keys per column.
       float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if constexpr (FP8) {
+        // f16 P: keys [32g, 32g+32) to columns [16g, 16g+16)
 #pragma unroll
-      for (int g = 0; g < BN / 16; ++g) {
+        for (int g = 0; g < BN / 32; ++g) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            const float p0 = ex2(fmaf(__uint_as_float(s[g * 32 + k]), p.scale_log2, -mref));
+            const float p1 = ex2(fmaf(__uint_as_float(s[g * 32 + k + 1]), p.scale_log2, -mref));
+            rs4[(k >> 1) & 3] += p0 + p1;
+            pk[k >> 1] = pack_f16(p0, p1);
+          }
+          tmem_st16(tS + g * 16, pk);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < (FP8 ? 0 : BN / 16); ++g) {
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; k += 2) {
@@ -442,7 +481,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ----------------------------------------------------------- epilogue
     if (ok && mbar_wait(&pv_done[t], (nkv - 1) & 1, p.wc, abort_flag, SITE_FWD_EPI)) {
       tc_fence_after();
-      const float inv_l = 1.0f / l;
+      float inv_l = 1.0f / l;
+      if constexpr (FP8) inv_l *= p.o_scale;
       const int q_sh = SHARDED ? q_idx / p.n_loc : 0;
       __nv_bfloat16 *orow = p.O + (int64_t)bh * p.o_sbh + (int64_t)q_sh * p.o_sshard +
                             (int64_t)(row0 + q_idx - q_sh * p.n_loc) * p.o_srow;
@@ -477,9 +517,57 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
+template <int D, bool SHARDED, bool VARLEN>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  attn_fwd_body<D, SHARDED, VARLEN, false>(tmQ, tmK, tmV, p);
+}
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  attn_fwd_body<D, false, false, true>(tmQ, tmK, tmV, p);
+}
+
+// e4m3 V [BHkv][n][128] (strided rows) -> f16 [BHkv][n][128] packed, each
+// value times 2^-8, exactly.  An e4m3 byte s.eeee.mmm placed as the f16 bit
+// pattern s.0eeee.mmm0000000 is the same number scaled by 2^(7-15): the f16
+// exponent bias is 15, e4m3's is 7, and e4m3 subnormals (e = 0) land on f16
+// subnormals with the same mantissa.  The NaN codes s.1111.111 become
+// +-1.875 (read as 480 after the epilogue's 2^8): inputs are taken finite.
+__global__ void __launch_bounds__(256)
+    v_e4m3_to_f16_kernel(const uint8_t *__restrict__ V, int64_t s_bh, int64_t s_row, int n,
+                         int64_t rows, uint16_t *__restrict__ out) {
+  const int64_t chunks = rows * 8;  // 16 e4m3 (16 bytes) per chunk
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < chunks;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i >> 3;
+    const int c = (int)(i & 7);
+    const int64_t h = r / n, t = r - h * n;
+    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(V + h * s_bh + t * s_row + c * 16));
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t y[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      // bytes (b0, b1) and (b2, b3) to the high byte of each 16-bit half
+      const uint32_t u0 = __byte_perm(w[k], 0, 0x1404);
+      const uint32_t u1 = __byte_perm(w[k], 0, 0x3424);
+      y[2 * k] = (u0 & 0x80008000u) | ((u0 >> 1) & 0x3F803F80u);
+      y[2 * k + 1] = (u1 & 0x80008000u) | ((u1 >> 1) & 0x3F803F80u);
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(out + r * 128 + c * 16);
+    dst[0] = make_uint4(y[0], y[1], y[2], y[3]);
+    dst[1] = make_uint4(y[4], y[5], y[6], y[7]);
+  }
+}
+
 template <int D>
 cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t st) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, false>;
   // Tensor maps {d, row, head} for one contiguous sequence; {d, row in
   // shard, shard, head} over sequence shards.
   CUtensorMap mq, mk, mv;
@@ -517,6 +605,7 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t s
   p.nkb = (a.n + BN - 1) / BN;
   p.causal = a.causal;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.o_scale = 1.0f;
   p.O = static_cast<__nv_bfloat16 *>(a.O);
   p.o_sbh = a.o_sbh;
   p.o_srow = a.o_srow;
@@ -543,6 +632,63 @@ cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs &a, const WaitCfg &wc, cudaSt
   if (a.d == 128) return launch_fwd_d<128>(a, wc, st);
   if (a.d == 64) return launch_fwd_d<64>(a, wc, st);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_fwd_fp8(const AttnFwdArgs &a, void *v16, const WaitCfg &wc,
+                               cudaStream_t st) {
+  if (a.d != 128 || a.n_loc != a.n || a.cu_seqlens) return cudaErrorNotSupported;
+  using L = FwdLayout<128, true>;
+  // V -> f16 (x 2^-8) into the workspace, [BHkv][n][128] packed
+  const int64_t rows = (int64_t)a.BHkv * a.n;
+  const int64_t blocks = (rows * 8 + 255) / 256;
+  timing_mark(st, 0);
+  v_e4m3_to_f16_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(
+      static_cast<const uint8_t *>(a.V), a.v_sbh, a.v_srow, a.n, rows,
+      static_cast<uint16_t *>(v16));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // Q, K: e4m3 rows of 128 bytes, one 128 x 128 box per tile; V: f16 boxes
+  // of 64 columns as in the bf16 kernel
+  CUtensorMap mq, mk, mv;
+  const uint32_t box_qk[3] = {128, 128, 1};
+  const uint32_t box_v[3] = {64, 128, 1};
+  const uint64_t dq[3] = {128, (uint64_t)a.n, (uint64_t)a.BH};
+  const uint64_t dkv[3] = {128, (uint64_t)a.n, (uint64_t)a.BHkv};
+  const uint64_t sq[2] = {(uint64_t)a.q_srow, (uint64_t)a.q_sbh};
+  const uint64_t sk[2] = {(uint64_t)a.k_srow, (uint64_t)a.k_sbh};
+  const uint64_t sv[2] = {256, (uint64_t)a.n * 256};
+  if ((e = make_tmap(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.Q, dq, sq, box_qk)) != cudaSuccess)
+    return e;
+  if ((e = make_tmap(&mk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.K, dkv, sk, box_qk)) != cudaSuccess)
+    return e;
+  if ((e = make_tmap(&mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, v16, dkv, sv, box_v)) != cudaSuccess)
+    return e;
+  FwdParams p;
+  p.BH = a.BH;
+  p.n = a.n;
+  p.cu = nullptr;
+  p.nbatch = 0;
+  p.nqb2 = (a.n + 2 * BM - 1) / (2 * BM);
+  p.nkb = (a.n + BN - 1) / BN;
+  p.causal = a.causal;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.o_scale = 256.0f * a.v_scale;
+  p.O = static_cast<__nv_bfloat16 *>(a.O);
+  p.o_sbh = a.o_sbh;
+  p.o_srow = a.o_srow;
+  p.o_sshard = 0;
+  p.n_loc = a.n;
+  p.G = a.BH / a.BHkv;
+  p.LSE = a.LSE;
+  p.lse_sbh = a.lse_sbh;
+  p.wc = wc;
+  e = cudaFuncSetAttribute(attn_fwd_fp8_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           L::ALLOC);
+  if (e != cudaSuccess) return e;
+  timing_mark(st, 1);
+  attn_fwd_fp8_kernel<128><<<(unsigned)(p.nqb2 * a.BH), NTHREADS, L::ALLOC, st>>>(mq, mk, mv, p);
+  timing_mark(st, 2);
+  return cudaGetLastError();
 }
 
 }  // namespace chain

@@ -101,7 +101,9 @@ struct View {
   int64_t s_row;   // elements between rows
 };
 
-int esize(int dtype) { return dtype == CHAIN_BF16 ? 2 : (dtype == CHAIN_F32 ? 4 : 0); }
+int esize(int dtype) {
+  return dtype == CHAIN_BF16 ? 2 : (dtype == CHAIN_F32 ? 4 : (dtype == CHAIN_E4M3 ? 1 : 0));
+}
 
 // Accepts 2-D [rows][cols], 3-D [BH][rows][cols] and 4-D [B][H][rows][cols]
 // where the two leading dims fold into one stride.
@@ -291,6 +293,7 @@ int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B, const chain_tens
       (rc = view_of(O, 2, &o)))
     return rc;
   if (a.dtype != b.dtype || a.dtype != c.dtype || a.dtype != o.dtype) return CHAIN_ERR_DTYPE;
+  if (a.dtype == CHAIN_E4M3) return CHAIN_ERR_DTYPE;  // 8-bit inputs: chain_fwd_fp8
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   if (f == CHAIN_F_SOFTMAX) {
@@ -637,6 +640,60 @@ int chain_bwd_varlen(const chain_tensor_t *dO, const chain_tensor_t *Q, const ch
   DevInfo *di = nullptr;
   if ((rc = device_ready(&di))) return rc;
   cudaError_t e = launch_attn_bwd(args, wait_cfg(di), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
+}
+
+static size_t fp8_ws_bytes(const View &v) {
+  return ((size_t)(v.outer * v.rows * v.cols * 2) + 255) & ~(size_t)255;
+}
+
+size_t chain_fwd_fp8_workspace_size(const chain_tensor_t *V) {
+  View v;
+  if (view_of(V, 2, &v) || v.dtype != CHAIN_E4M3) return 0;
+  return fp8_ws_bytes(v);
+}
+
+int chain_fwd_fp8(const chain_tensor_t *Q, const chain_tensor_t *K, const chain_tensor_t *V,
+                  int mask, float scale, float v_scale, chain_tensor_t *O, chain_tensor_t *LSE,
+                  void *workspace, size_t ws_bytes, void *stream) {
+  if (mask != CHAIN_MASK_NONE && mask != CHAIN_MASK_CAUSAL) return CHAIN_ERR_ARG;
+  View q, k, v, o;
+  int rc;
+  if ((rc = view_of(Q, 2, &q)) || (rc = view_of(K, 2, &k)) || (rc = view_of(V, 2, &v)) ||
+      (rc = view_of(O, 2, &o)))
+    return rc;
+  if (q.dtype != CHAIN_E4M3 || k.dtype != CHAIN_E4M3 || v.dtype != CHAIN_E4M3 ||
+      o.dtype != CHAIN_BF16)
+    return CHAIN_ERR_DTYPE;
+  if (!kv_shape(q, k) || !same_shape(k, v) || !same_shape(q, o)) return CHAIN_ERR_ARG;
+  if (q.rows < 1 || q.outer < 1) return CHAIN_ERR_ARG;
+  if (q.rows > (1 << 30) || q.outer > 65535 * 16) return CHAIN_ERR_ARG;
+  if (q.cols != 128) return q.cols == 64 ? CHAIN_ERR_UNSUPPORTED : CHAIN_ERR_ARG;
+  if (!(scale > 0.0f) || !(scale < 1e30f)) return CHAIN_ERR_ARG;
+  if (!(v_scale == v_scale) || !(v_scale < 1e30f) || !(v_scale > -1e30f)) return CHAIN_ERR_ARG;
+  if (!pitch16(q) || !pitch16(k) || !pitch16(v) || !pitch16(o)) return CHAIN_ERR_ARG;
+  int64_t lse_sbh = 0;
+  if ((rc = lse_view(LSE, q.outer, q.rows, &lse_sbh))) return rc;
+  if (!workspace || !aligned16(workspace) || ws_bytes < fp8_ws_bytes(v)) return CHAIN_ERR_ARG;
+  AttnFwdArgs args;
+  args.Q = q.ptr; args.K = k.ptr; args.V = v.ptr;
+  args.q_sbh = q.s_outer; args.q_srow = q.s_row;
+  args.k_sbh = k.s_outer; args.k_srow = k.s_row;
+  args.v_sbh = v.s_outer; args.v_srow = v.s_row;
+  args.O = o.ptr; args.o_sbh = o.s_outer; args.o_srow = o.s_row;
+  args.LSE = static_cast<float *>(LSE->ptr); args.lse_sbh = lse_sbh;
+  args.BH = (int)q.outer; args.n = (int)q.rows; args.d = 128;
+  args.BHkv = (int)k.outer;
+  args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
+  args.v_scale = v_scale;
+  args.n_loc = args.n;
+  args.q_sshard = args.k_sshard = args.v_sshard = args.o_sshard = 0;
+  args.cu_seqlens = nullptr; args.nbatch = 0; args.max_seqlen = 0;
+  DevInfo *di = nullptr;
+  if ((rc = device_ready(&di))) return rc;
+  cudaError_t e = launch_attn_fwd_fp8(args, workspace, wait_cfg(di),
+                                      static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return CHAIN_ERR_UNSUPPORTED;
   return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
 }
 

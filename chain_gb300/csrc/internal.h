@@ -33,9 +33,14 @@ struct AttnFwdArgs {
   // packed rows (n = total rows), or null.
   const int *cu_seqlens;
   int nbatch, max_seqlen;
+  float v_scale = 1.0f;  // e4m3 inputs: the factor V's codes are multiplied by
 };
 
 cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t st);
+// e4m3 Q, K, V (d = 128, dense); v16 = 2 x BHkv x n x 128 bytes of workspace
+// (16-byte aligned) for the f16 copy of V.
+cudaError_t launch_attn_fwd_fp8(const AttnFwdArgs &a, void *v16, const WaitCfg &wc,
+                               cudaStream_t st);
 cudaError_t launch_attn_fwd_f32(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t st);
 
 struct AttnBwdArgs {

@@ -7,7 +7,7 @@ method's arithmetic.
 Seeds: workload k (1-based, in the order of ``WORKLOADS``) draws with seed
 ``1000*k + offset``, offsets Q/X +0, K/W1 +1, V/W2 +2, dO +3.  Values are
 drawn in fp32 (``torch.randn``) and rounded to bf16 (round-to-nearest-even)
-where the workload is bf16.
+where the workload is bf16, to the nearest e4m3 value where it is e4m3.
 """
 from __future__ import annotations
 
@@ -46,6 +46,10 @@ WORKLOADS = {
                                   dtype="bf16")),
     "causal_bwd_64k": Workload("causal_bwd_64k", 5, "attn_bwd",
                                dict(BH=16, n=65536, d=128, causal=True, dtype="bf16")),
+    # the causal 32k forward with Q, K, V stored as e4m3 (fp32 draws rounded
+    # to the nearest e4m3 value)
+    "causal_attn_32k_e4m3": Workload("causal_attn_32k_e4m3", 6, "attn_fwd",
+                                     dict(BH=32, n=32768, d=128, causal=True, dtype="e4m3")),
 }
 
 

@@ -59,7 +59,9 @@ typedef enum {
   CHAIN_ERR_SCRATCH_LIMIT = -7 /* problem needs more than CHAIN_NOALLOC_SCRATCH_BYTES */
 } chain_status_t;
 
-typedef enum { CHAIN_BF16 = 0, CHAIN_F32 = 1 } chain_dtype_t;
+/* CHAIN_E4M3: 8-bit float, 1 sign, 4 exponent (bias 7) and 3 mantissa bits,
+ * no infinities, S.1111.111 = NaN; largest finite value 448. */
+typedef enum { CHAIN_BF16 = 0, CHAIN_F32 = 1, CHAIN_E4M3 = 2 } chain_dtype_t;
 
 typedef enum {
   CHAIN_F_IDENTITY = 0,  /* O = (A B) C */
@@ -270,12 +272,43 @@ int chain_bwd_varlen(const chain_tensor_t *dO, const chain_tensor_t *Q,
                      chain_tensor_t *dV, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * chain_fwd_fp8 -- softmax attention, O = softmax(scale Q K^T) (v_scale V),
+ * on 8-bit float inputs: the unit O = f(A B) C of "Memory-efficient tensor
+ * parallelism" (FITEE 10.1631/FITEE.2400602, abstract) with f = row softmax,
+ * read from e4m3 tensors.  The pages define no 8-bit variant: this entry
+ * stores the three inputs in half the bytes of bf16 and runs the Q K^T
+ * product at the 8-bit tensor-core rate.
+ *   Q  [BH][n][128], K, V  [BHkv][n][128] CHAIN_E4M3 (3-D, or 4-D with B*H
+ *      folded), BHkv dividing BH (grouped-query attention as in chain_fwd);
+ *      rows contiguous, row and head strides multiples of 16 bytes.
+ *   scale    multiplies Q K^T in fp32 (fold Q's and K's dequantisation
+ *            factors into it); > 0 and finite.
+ *   v_scale  V's dequantisation factor, applied to O in fp32; finite.
+ *   O        [BH][n][128] bf16;  LSE [BH][n] fp32, natural log, scale included.
+ *   mask     as for chain_fwd.
+ *   workspace  at least chain_fwd_fp8_workspace_size(V) bytes (2 * BHkv * n *
+ *            128, rounded up to 256), 16-byte aligned: V re-encoded as f16
+ *            (exactly: every e4m3 value is an f16 value times 2^8).
+ * Arithmetic: the Q K^T products of e4m3 values are exact, accumulated in
+ * fp32; P enters the P V product as f16 (11 significant bits) with V's exact
+ * f16 copy; fp32 accumulation; one bf16 rounding of O.  Inputs must be finite
+ * (a NaN code is read as +-480).  Returns CHAIN_ERR_DTYPE unless Q, K, V are
+ * e4m3 and O bf16, CHAIN_ERR_UNSUPPORTED for d != 128, CHAIN_ERR_ARG for a
+ * shape, stride, alignment or workspace violation.  Asynchronous on `stream`.
+ */
+size_t chain_fwd_fp8_workspace_size(const chain_tensor_t *V);
+int chain_fwd_fp8(const chain_tensor_t *Q, const chain_tensor_t *K,
+                  const chain_tensor_t *V, int mask, float scale, float v_scale,
+                  chain_tensor_t *O, chain_tensor_t *LSE, void *workspace,
+                  size_t ws_bytes, void *stream);
+
+/*
  * sp_relayout -- Ulysses sequence shards -> head-major for one head group
  * ("Ulysses Sequence Parallelism", "Contexte Technique": every position of
  * the sequence, a subset of the heads).
  *   shards [p][n_loc][H][d]: shard s holds positions [s*n_loc, (s+1)*n_loc).
  *   out    [H/p][p*n_loc][d]: out[h][s*n_loc+t][e] = shards[s][t][g*H/p+h][e]
- *   with g = head_group in [0, p).  Bit-exact copy of any 2- or 4-byte
+ *   with g = head_group in [0, p).  Bit-exact copy of any 1-, 2- or 4-byte
  *   element type; d * element size must be a multiple of 16 bytes.
  */
 int sp_relayout(const chain_tensor_t *shards, int p, int head_group,

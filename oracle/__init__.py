@@ -7,7 +7,8 @@ product path (``chain_gb300``) never touches it.
 This module only marshals arguments into ``oracle.c`` (plain C, fp64,
 OpenMP); every step of the arithmetic lives there, written from the
 definitions cited in its header.  Inputs are torch CPU tensors or numpy
-arrays holding bf16, fp32 or fp64 values; outputs are fp64 numpy arrays.
+arrays holding bf16, e4m3, fp32 or fp64 values; outputs are fp64 numpy
+arrays.
 """
 from __future__ import annotations
 
@@ -24,7 +25,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-BF16, F32, F64 = 0, 1, 2
+BF16, F32, F64, E4M3 = 0, 1, 2, 3
 F_IDENTITY, F_SOFTMAX, F_GELU_TANH = 0, 1, 2
 
 
@@ -60,6 +61,8 @@ def _load():
             lib.oracle_chain_bwd.argtypes = [ci, vp, vp, vp, vp, i64, i64, i64, i64, ci, i64, vp,
                                              i64, vp, vp, vp, vp]
             lib.oracle_relayout.argtypes = [vp, i64, i64, i64, i64, i64, i64, vp]
+            lib.oracle_e4m3_decode.argtypes = [vp, i64, vp]
+            lib.oracle_e4m3_decode.restype = None
             lib.oracle_relayout_inverse.argtypes = [vp, i64, i64, i64, i64, i64, i64, vp]
             for fn in ("oracle_softmax_fwd", "oracle_softmax_fwd_blocked", "oracle_softmax_bwd",
                        "oracle_chain_fwd", "oracle_chain_bwd", "oracle_relayout",
@@ -85,6 +88,8 @@ def _raw(x):
                 return x.numpy(), F32
             if x.dtype == torch.float64:
                 return x.numpy(), F64
+            if x.dtype == torch.float8_e4m3fn:
+                return x.view(torch.uint8).numpy(), E4M3
             raise TypeError(f"oracle: unsupported dtype {x.dtype}")
     except ImportError:  # pragma: no cover
         pass
@@ -105,6 +110,23 @@ def _same(*arrs):
 
 def _p(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """float64 values of e4m3 codes (uint8 array or torch float8_e4m3fn)."""
+    try:
+        import torch
+        if isinstance(codes, torch.Tensor):
+            codes = codes.detach().cpu().contiguous()
+            if codes.dtype == torch.float8_e4m3fn:
+                codes = codes.view(torch.uint8)
+            codes = codes.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _load().oracle_e4m3_decode(_p(c), int(c.size), _p(out))
+    return out
 
 
 def softmax_fwd(Q, K, V, scale: float, causal: bool, rows=None):

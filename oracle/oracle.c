@@ -9,8 +9,8 @@
  * Every function computes the plain definition, materialising what the GPU
  * path never materialises (full score rows, the full hidden activation row),
  * with no blocking, fusion or reordering beyond what the definition states.
- * Inputs are read as stored (bf16 bit patterns, fp32 or fp64) and widened
- * exactly to double; all arithmetic is double.
+ * Inputs are read as stored (bf16 or e4m3 bit patterns, fp32 or fp64) and
+ * widened exactly to double; all arithmetic is double.
  *
  * Sources (page titles of the method's write-ups):
  *  - "Memory-efficient tensor parallelism" (FITEE 10.1631/FITEE.2400602),
@@ -46,14 +46,35 @@
 #define ORACLE_BF16 0
 #define ORACLE_F32 1
 #define ORACLE_F64 2
+#define ORACLE_E4M3 3
 
 #define ORACLE_F_IDENTITY 0
 #define ORACLE_F_SOFTMAX 1
 #define ORACLE_F_GELU_TANH 2
 
+/* The 8-bit float e4m3 from its definition: sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits; exponent field 0 is subnormal (2^-6 * m/8); no
+ * infinities; exponent 15 with mantissa 7 is NaN. */
+static double e4m3_value(uint8_t b) {
+  const int s = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  double v;
+  if (e == 15 && m == 7)
+    v = NAN;
+  else if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+void oracle_e4m3_decode(const uint8_t *in, int64_t count, double *out) {
+  for (int64_t i = 0; i < count; ++i) out[i] = e4m3_value(in[i]);
+}
+
 /* Exact widening of one stored element to double.  A bf16 value is the top
  * 16 bits of an IEEE binary32, so shifting the pattern up reproduces it. */
 static double elem(const void *base, int dtype, int64_t i) {
+  if (dtype == ORACLE_E4M3) return e4m3_value(((const uint8_t *)base)[i]);
   if (dtype == ORACLE_BF16) {
     uint32_t bits = ((uint32_t)((const uint16_t *)base)[i]) << 16;
     float f;

@@ -369,3 +369,48 @@ def test_relayout_round_trip(orc):
         orc.relayout_inverse(torch.from_numpy(out.view(np.int16).reshape(shape)), p, n_loc, H,
                              g, into=back)
     assert np.array_equal(back, x.view(torch.uint8).numpy().reshape(-1))
+
+
+# ------------------------------------------------------------ e4m3 inputs
+def test_e4m3_decode_closed_forms(orc):
+    # values the format fixes: sign, 4 exponent bits with bias 7, 3 mantissa
+    # bits, exponent field 0 subnormal, S.1111.111 NaN
+    cases = {0x00: 0.0, 0x38: 1.0, 0x40: 2.0, 0x3C: 1.5, 0xB8: -1.0, 0x30: 0.5,
+             0x7E: 448.0, 0xFE: -448.0, 0x77: 240.0, 0x08: 2.0 ** -6, 0x01: 2.0 ** -9,
+             0x07: 7 * 2.0 ** -9, 0x81: -(2.0 ** -9)}
+    codes = np.array(list(cases), dtype=np.uint8)
+    got = orc.e4m3_decode(codes)
+    assert list(got) == [cases[int(c)] for c in codes]
+    assert np.isnan(orc.e4m3_decode(np.array([0x7F, 0xFF], np.uint8))).all()
+
+
+def test_e4m3_decode_matches_torch(orc):
+    # every code against the library's float8_e4m3fn conversion
+    codes = np.arange(256, dtype=np.uint8)
+    ours = orc.e4m3_decode(codes)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float32).double().numpy()
+    nan = np.isnan(ref)
+    assert set(np.flatnonzero(nan).tolist()) == {0x7F, 0xFF}
+    np.testing.assert_array_equal(np.isnan(ours), nan)
+    np.testing.assert_array_equal(ours[~nan], ref[~nan])
+
+
+def test_e4m3_decode_monotone_and_odd(orc):
+    pos = orc.e4m3_decode(np.arange(0x00, 0x7F, dtype=np.uint8))
+    neg = orc.e4m3_decode(np.arange(0x80, 0xFF, dtype=np.uint8))
+    assert np.all(np.diff(pos) > 0)
+    np.testing.assert_array_equal(neg, -pos)
+
+
+def test_oracle_softmax_on_e4m3_codes(orc):
+    # the oracle fed e4m3 codes computes on their exact values: identical to
+    # feeding those values in fp64, and to the library's scaled-dot-product
+    # attention on them
+    q, k, v = cs.attn_inputs(2, 40, 8, seed=61, dtype=torch.float8_e4m3fn)
+    O8, L8 = orc.softmax_fwd(q, k, v, 0.3, True)
+    dec = [torch.from_numpy(orc.e4m3_decode(x)) for x in (q, k, v)]
+    O64, L64 = orc.softmax_fwd(*dec, 0.3, True)
+    np.testing.assert_array_equal(O8, O64)
+    np.testing.assert_array_equal(L8, L64)
+    ref = torch.nn.functional.scaled_dot_product_attention(*dec, is_causal=True, scale=0.3)
+    assert rel(O8, ref.numpy()) < TIGHT
