@@ -9,7 +9,7 @@
 // One CTA per (head, 256-row query block) = two 128-row query tiles "a" and
 // "b" that share every K/V tile; CTAs run head by head (K/V reuse in L2),
 // heaviest causal blocks first within a head.
-// Warp roles (320 threads):
+// Warp roles (320 threads; 384 for 8-bit inputs, warps 10 and 11 idle):
 //   warps 0-3  softmax of tile a, warps 4-7 softmax of tile b: thread t of
 //              a warpgroup owns query row t of its tile.  It reads its row
 //              of S from tensor memory, runs the online softmax in fp32
@@ -46,7 +46,17 @@ namespace {
 constexpr int BM = 128;  // rows per query tile (two tiles per CTA)
 constexpr int BN = 128;  // keys per K/V tile
 constexpr int STAGES = 2;
-constexpr int NTHREADS = 320;
+// Threads a CTA: 320 for bf16 (8 softmax warps, producer, MMA; 168
+// registers, three warps per scheduler filling its quarter of the register
+// file).  For 8-bit inputs 384 at 168 registers (384 x 168 = 64,512 of the
+// SM's 65,536): the producer/MMA warpgroup (with two idle warps) gives back
+// down to 136 and the softmax warpgroups take 184, so that a row of S stays
+// in registers next to the packed arithmetic's register pairs:
+// 256 x 184 + 128 x 136 = 64,512, and 184 + 184 + 136 <= 512 per scheduler.
+// (The same split measured 2-3% slower for bf16 at n = 131072.)
+template <bool FP8>
+constexpr int fwd_threads() { return FP8 ? 384 : 320; }
+constexpr uint32_t REGS_SOFTMAX = 184, REGS_CONTROL = 136;  // 8-bit inputs
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 
 template <int D, bool FP8>
@@ -204,7 +214,9 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  // The three roles; 8-bit inputs reallocate registers per warpgroup
+  // before running theirs.
+  auto role_producer = [&]() {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       int k_issued = 0, v_issued = 0;
@@ -260,7 +272,8 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
+  };
+  auto role_mma = [&]() {
     // --------------------------------------------------------- MMA issuer
     // The whole warp runs the loop; one elected lane issues each group of
     // products together with its commits.
@@ -369,7 +382,8 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
       if (lane == 0) drain_wait(mma_drain, 0, p.wc);
     }
     __syncwarp();
-  } else {
+  };
+  auto role_softmax = [&]() {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;            // query tile of this warpgroup
     const int row = threadIdx.x & 127;  // tensor-memory lane = row
@@ -405,12 +419,25 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
         }
       }
       // pass 1: row max, eight independent partial maxima (a tree, not a
-      // 128-long dependent chain)
+      // 128-long dependent chain); 8-bit inputs: four, two keys per
+      // three-input max
       float mx8[8];
+      if constexpr (FP8) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(s[u]);
+        for (int u = 0; u < 4; ++u)
+          mx8[u] = fmaxf(__uint_as_float(s[2 * u]), __uint_as_float(s[2 * u + 1]));
 #pragma unroll
-      for (int k = 8; k < BN; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(s[k]));
+        for (int k = 8; k < BN; k += 8)
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            mx8[u] = fmax3(mx8[u], __uint_as_float(s[k + 2 * u]), __uint_as_float(s[k + 2 * u + 1]));
+        mx8[4] = mx8[5] = mx8[6] = mx8[7] = -INFINITY;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(s[u]);
+#pragma unroll
+        for (int k = 8; k < BN; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(s[k]));
+      }
       float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       mx *= p.scale_log2;  // scale > 0: the max commutes with the scaling
@@ -429,18 +456,30 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
       // [16g, 16g+8) (P_hi) and [16g+8, 16g+16) (P_lo), two keys per column.
       float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       if constexpr (FP8) {
-        // f16 P: keys [32g, 32g+32) to columns [16g, 16g+16)
+        // f16 P: keys [32g, 32g+32) to columns [16g, 16g+16); two keys per
+        // packed fp32 instruction for x = s * scale - m and the row sum
+        const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2);
+        const uint64_t nm2 = f32x2(-mref, -mref);
+        uint64_t rs2[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int g = 0; g < BN / 32; ++g) {
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 32; k += 2) {
-            const float p0 = ex2(fmaf(__uint_as_float(s[g * 32 + k]), p.scale_log2, -mref));
-            const float p1 = ex2(fmaf(__uint_as_float(s[g * 32 + k + 1]), p.scale_log2, -mref));
-            rs4[(k >> 1) & 3] += p0 + p1;
+            float x0, x1;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(s[g * 32 + k]),
+                                        __uint_as_float(s[g * 32 + k + 1])), sc2, nm2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            rs2[(k >> 1) & 3] = add_f32x2(rs2[(k >> 1) & 3], f32x2(p0, p1));
             pk[k >> 1] = pack_f16(p0, p1);
           }
           tmem_st16(tS + g * 16, pk);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float a0, a1;
+          f32x2_split(rs2[u], a0, a1);
+          rs4[u] = a0 + a1;
         }
       }
 #pragma unroll
@@ -507,6 +546,25 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
       if (q_idx < n)
         p.LSE[(int64_t)bh * p.lse_sbh + row0 + q_idx] = (m + lg2(l)) * 0.69314718055994531f;
     }
+  };
+  if constexpr (FP8) {
+    if (warp >= 8) {  // warps 10 and 11 only hand their registers over
+      setmaxnreg_dec<REGS_CONTROL>();
+      if (warp == 8)
+        role_producer();
+      else if (warp == 9)
+        role_mma();
+    } else {
+      setmaxnreg_inc<REGS_SOFTMAX>();
+      role_softmax();
+    }
+  } else {
+    if (warp == 8)
+      role_producer();
+    else if (warp == 9)
+      role_mma();
+    else
+      role_softmax();
   }
 
   tc_fence_before();
@@ -518,7 +576,7 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
 }
 
 template <int D, bool SHARDED, bool VARLEN>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(fwd_threads<false>(), 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -526,7 +584,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 template <int D>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(fwd_threads<true>(), 1)
     attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -621,7 +679,7 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t s
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(p.nqb2 * a.BH * (a.cu_seqlens ? a.nbatch : 1));
   timing_mark(st, 0);
-  kern<<<grid, NTHREADS, L::ALLOC, st>>>(mq, mk, mv, p);
+  kern<<<grid, fwd_threads<false>(), L::ALLOC, st>>>(mq, mk, mv, p);
   timing_mark(st, 1);
   return cudaGetLastError();
 }
@@ -686,7 +744,8 @@ cudaError_t launch_attn_fwd_fp8(const AttnFwdArgs &a, void *v16, const WaitCfg &
                            L::ALLOC);
   if (e != cudaSuccess) return e;
   timing_mark(st, 1);
-  attn_fwd_fp8_kernel<128><<<(unsigned)(p.nqb2 * a.BH), NTHREADS, L::ALLOC, st>>>(mq, mk, mv, p);
+  attn_fwd_fp8_kernel<128>
+      <<<(unsigned)(p.nqb2 * a.BH), fwd_threads<true>(), L::ALLOC, st>>>(mq, mk, mv, p);
   timing_mark(st, 2);
   return cudaGetLastError();
 }
