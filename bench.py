@@ -565,7 +565,9 @@ def measure_fp8(hp, reps=5):
         "roofline": {"bound": "tensor", "kernel": "attn_fwd_fp8_kernel", "achieved": round(ka, 1),
                      "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(ka / peak, 4),
                      "peak_basis": f"4/3 x {src} sustained bf16 (Q K^T at the nominal 2x "
-                                   "8-bit rate, P V at the 16-bit rate)"},
+                                   "8-bit rate, P V at the 16-bit rate)",
+                     "traffic": measured_traffic("attn_fwd_fp8_kernel"),
+                     "traffic_unit": "bytes per launch (ncu)"},
         "inputs": "e4m3 Q, K, V (fp32 N(0,1) draws rounded to e4m3), O bf16",
         "timing": f"median of {reps} after 2 warm-ups; inputs larger than L2"}}
 
