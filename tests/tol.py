@@ -6,6 +6,8 @@ and mean relative error sum|O - O_ref| / sum|O_ref| <= 2e-3.  Gradients:
 LSE (fp32, natural log): |LSE - LSE_ref| <= 1e-3 absolute (derivation in
 the design notes: fp32 score accumulation and ex2/lg2 approximation errors
 are ~1e-5; bf16 rounding of P does not enter the LSE).
+The e4m3-input forward is held to the same bounds against the oracle fed the
+same codes (their exact values): its P is f16, its O one bf16 rounding.
 """
 import numpy as np
 
