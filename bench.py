@@ -6,7 +6,9 @@ number):
   * sp_relayout of the Q, K and V sequence shards 4x[32768][32][128] bf16
     to head-major [8][131072][128] (head group 0),
   * causal attention forward on those 8 heads at n = 131072, d = 128,
-  * causal attention forward 32 x 32768 x 128,
+  * causal attention forward 32 x 32768 x 128 (both through chain_fwd_f16pv:
+    P V as one f16 product, V re-encoded by a two-launch pre-pass that is
+    timed with them; chain_fwd's compensated form is timed beside the step),
   * GeLU MLP chain 4096x1024 . 1024x4096 . 4096x1024,
   * causal attention backward with recompute 16 x 65536 x 128,
   * the small fp32 attention 1 x 256 x 64.
@@ -170,8 +172,10 @@ class HotPath:
                 cg.sp_relayout(self.shards[t], u["p"], u["g"], self.hm[t])
             self.o4 = torch.empty(Hl, N, u["d"], dtype=torch.bfloat16, device=dev)
             self.l4 = torch.empty(Hl, N, dtype=torch.float32, device=dev)
+            self.ws4 = torch.empty(cg.chain_fwd_f16pv_workspace_size(self.hm[0], self.hm[2]),
+                                   dtype=torch.uint8, device=dev)
         else:
-            self.shards, self.hm, self.o4, self.l4 = [e] * 3, [e] * 3, e, e
+            self.shards, self.hm, self.o4, self.l4, self.ws4 = [e] * 3, [e] * 3, e, e, e
         c3 = W["causal_attn_32k"].dims
         self.c3 = c3
         if want("attn_fwd_causal_32x32768x128"):
@@ -179,8 +183,10 @@ class HotPath:
                                                        seed=g("causal_attn_32k"), device=dev)
             self.o3 = torch.empty_like(self.q3)
             self.l3 = torch.empty(c3["BH"], c3["n"], dtype=torch.float32, device=dev)
+            self.ws3 = torch.empty(cg.chain_fwd_f16pv_workspace_size(self.q3, self.v3),
+                                   dtype=torch.uint8, device=dev)
         else:
-            self.q3 = self.k3 = self.v3 = self.o3 = self.l3 = e
+            self.q3 = self.k3 = self.v3 = self.o3 = self.l3 = self.ws3 = e
         m = W["gelu_mlp"].dims
         self.m = m
         if want("gelu_mlp"):
@@ -247,17 +253,25 @@ class HotPath:
                               bytes=2.0 * Hl * N * u["d"] * 2, launches=1,
                               kernels=[("relayout_kernel", 0.0, 2.0 * Hl * N * u["d"] * 2)],
                               fn=(lambda t=t: cg.sp_relayout(self.shards[t], u["p"], u["g"], self.hm[t]))))
+        # the causal forwards: chain_fwd_f16pv (P V as one f16 product); its
+        # V pre-pass (two HBM-bound launches: 2 + 2 bytes read, 2 written per
+        # element) is timed with it
+        pre = "v_absmax_kernel+v_to_f16_kernel"
         comps.append(dict(name="attn_fwd_causal_8x131072x128", flops=attn_fwd_flops(Hl, N, u["d"], True),
-                          bytes=0.0, launches=1,
-                          kernels=[("attn_fwd_kernel", attn_fwd_flops(Hl, N, u["d"], True), 0.0)],
-                          fn=lambda: cg.chain_fwd(self.hm[0], self.hm[1], self.hm[2], cg.F_SOFTMAX,
-                                                  cg.MASK_CAUSAL, u["d"] ** -0.5, self.o4, self.l4)))
+                          bytes=0.0, launches=3,
+                          kernels=[(pre, 0.0, 6.0 * Hl * N * u["d"]),
+                                   ("attn_fwd_pv16_kernel", attn_fwd_flops(Hl, N, u["d"], True), 0.0)],
+                          fn=lambda: cg.chain_fwd_f16pv(self.hm[0], self.hm[1], self.hm[2],
+                                                        cg.MASK_CAUSAL, u["d"] ** -0.5, self.o4,
+                                                        self.l4, self.ws4)))
         comps.append(dict(name="attn_fwd_causal_32x32768x128",
-                          flops=attn_fwd_flops(c3["BH"], c3["n"], c3["d"], True), bytes=0.0, launches=1,
-                          kernels=[("attn_fwd_kernel", attn_fwd_flops(c3["BH"], c3["n"], c3["d"], True),
-                                    0.0)],
-                          fn=lambda: cg.chain_fwd(self.q3, self.k3, self.v3, cg.F_SOFTMAX,
-                                                  cg.MASK_CAUSAL, c3["d"] ** -0.5, self.o3, self.l3)))
+                          flops=attn_fwd_flops(c3["BH"], c3["n"], c3["d"], True), bytes=0.0, launches=3,
+                          kernels=[(pre, 0.0, 6.0 * c3["BH"] * c3["n"] * c3["d"]),
+                                   ("attn_fwd_pv16_kernel",
+                                    attn_fwd_flops(c3["BH"], c3["n"], c3["d"], True), 0.0)],
+                          fn=lambda: cg.chain_fwd_f16pv(self.q3, self.k3, self.v3, cg.MASK_CAUSAL,
+                                                        c3["d"] ** -0.5, self.o3, self.l3,
+                                                        self.ws3)))
         if self.mlp_ok:
             comps.append(dict(name="gelu_mlp_4096x1024x4096x1024",
                               flops=mlp_flops(m["M"], m["K"], m["N"], m["P"]), bytes=0.0, launches=1,
@@ -572,6 +586,48 @@ def measure_fp8(hp, reps=5):
         "timing": f"median of {reps} after 2 warm-ups; inputs larger than L2"}}
 
 
+def measure_fwd_compensated(hp, reps=5):
+    """The causal forwards of the step through chain_fwd (P V as the
+    compensated bf16 pair, no workspace), timed beside the step."""
+    torch, cg = hp.torch, hp.cg
+    out = {}
+    cases = []
+    if hp.q3.numel():
+        cases.append(("attn_fwd_compensated_causal_32x32768x128", hp.q3, hp.k3, hp.v3, hp.o3,
+                      hp.l3))
+    if hp.hm[0].numel():
+        cases.append(("attn_fwd_compensated_causal_8x131072x128", hp.hm[0], hp.hm[1], hp.hm[2],
+                      hp.o4, hp.l4))
+    for name, q, k, v, o, l in cases:
+        d = q.shape[-1]
+
+        def run(evs=None):
+            if evs is not None:
+                cg.set_timing_events(*evs)
+            cg.chain_fwd(q, k, v, cg.F_SOFTMAX, cg.MASK_CAUSAL, d ** -0.5, o, l)
+            if evs is not None:
+                cg.set_timing_events()
+
+        for _ in range(2):
+            run()
+        ts = []
+        for _ in range(reps):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            torch.cuda.synchronize()
+            run(evs)
+            torch.cuda.synchronize()
+            ts.append(evs[0].elapsed_time(evs[1]))
+        rc, site = cg.chain_check()
+        if rc != 0:
+            raise RuntimeError(f"device status {rc} site {site:#x} in the chain_fwd measurement")
+        med = sorted(ts)[len(ts) // 2]
+        fl = attn_fwd_flops(q.shape[0], q.shape[1], d, True)
+        out[name] = {"ms": round(med, 4), "TFLOPs": round(fl / (med * 1e-3) / 1e12, 1),
+                     "kernel": "attn_fwd_kernel (chain_fwd)",
+                     "timing": f"median of {reps} after 2 warm-ups"}
+    return out
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -770,6 +826,8 @@ def main():
         nxt.update(measure_mlp_bwd(hp))
     if args.only is None or "fp8" in args.only:
         nxt.update(measure_fp8(hp))
+    if hp.q3.numel() or hp.hm[0].numel():
+        nxt.update(measure_fwd_compensated(hp))
     nxt = nxt or None
 
     cpu = None

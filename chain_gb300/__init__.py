@@ -77,6 +77,9 @@ def _load():
             lib.chain_bwd_varlen.argtypes = [P, P, P, P, P, P, vp, ci, ci, ci, fl, P, P, P, vp,
                                              ctypes.c_size_t, vp]
             lib.chain_fwd_fp8.argtypes = [P, P, P, ci, fl, fl, P, P, vp, ctypes.c_size_t, vp]
+            lib.chain_fwd_f16pv.argtypes = [P, P, P, ci, fl, P, P, vp, ctypes.c_size_t, vp]
+            lib.chain_fwd_f16pv_workspace_size.argtypes = [P, P]
+            lib.chain_fwd_f16pv_workspace_size.restype = ctypes.c_size_t
             lib.chain_fwd_fp8_workspace_size.argtypes = [P]
             lib.chain_fwd_fp8_workspace_size.restype = ctypes.c_size_t
             lib.sp_relayout.argtypes = [P, ci, ci, P, vp]
@@ -91,7 +94,7 @@ def _load():
             lib.chain_status_string.argtypes = [ci]
             lib.chain_status_string.restype = ctypes.c_char_p
             for fn in ("chain_fwd", "chain_fwd_sp", "chain_fwd_varlen", "chain_bwd", "chain_bwd_varlen",
-                       "chain_bwd_noalloc", "chain_fwd_fp8",
+                       "chain_bwd_noalloc", "chain_fwd_fp8", "chain_fwd_f16pv",
                        "sp_relayout",
                        "sp_relayout_inverse",
                        "chain_check", "chain_selftest_wait_timeout", "chain_umma_selftest",
@@ -168,6 +171,19 @@ def chain_fwd_fp8(Q, K, V, mask, scale, v_scale, O, LSE, workspace, stream=None)
                               ctypes.c_void_p(workspace.data_ptr()),
                               workspace.numel() * workspace.element_size(), _stream(stream)),
         "chain_fwd_fp8")
+
+
+def chain_fwd_f16pv(Q, K, V, mask, scale, O, LSE, workspace, stream=None):
+    """Softmax attention, bf16, P V as one f16 product; see include/chain.h."""
+    _ok(_load().chain_fwd_f16pv(_ref(desc(Q)), _ref(desc(K)), _ref(desc(V)), int(mask),
+                                float(scale), _ref(desc(O)), _ref(desc(LSE)),
+                                ctypes.c_void_p(workspace.data_ptr()),
+                                workspace.numel() * workspace.element_size(), _stream(stream)),
+        "chain_fwd_f16pv")
+
+
+def chain_fwd_f16pv_workspace_size(Q, V) -> int:
+    return int(_load().chain_fwd_f16pv_workspace_size(_ref(desc(Q)), _ref(desc(V))))
 
 
 def chain_fwd_fp8_workspace_size(V) -> int:
@@ -283,6 +299,19 @@ def attention_fwd(q, k, v, causal: bool, scale: float | None = None, stream=None
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     chain_fwd(q, k, v, F_SOFTMAX, MASK_CAUSAL if causal else MASK_NONE, scale, o, lse, stream)
+    return o, lse
+
+
+def attention_fwd_f16pv(q, k, v, causal: bool, scale: float | None = None, workspace=None,
+                        stream=None):
+    """Returns (O, LSE) for bf16 q [BH, n, d], k, v [BHkv, n, d]; P V in f16."""
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(max(chain_fwd_f16pv_workspace_size(q, v), 16), dtype=torch.uint8,
+                                device=q.device)
+    chain_fwd_f16pv(q, k, v, MASK_CAUSAL if causal else MASK_NONE, scale, o, lse, workspace, stream)
     return o, lse
 
 

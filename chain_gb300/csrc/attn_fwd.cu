@@ -54,14 +54,14 @@ constexpr int STAGES = 2;
 // in registers next to the packed arithmetic's register pairs:
 // 256 x 184 + 128 x 136 = 64,512, and 184 + 184 + 136 <= 512 per scheduler.
 // (The same split measured 2-3% slower for bf16 at n = 131072.)
-template <bool FP8>
-constexpr int fwd_threads() { return FP8 ? 384 : 320; }
+template <bool PV16>
+constexpr int fwd_threads() { return PV16 ? 384 : 320; }
 constexpr uint32_t REGS_SOFTMAX = 184, REGS_CONTROL = 136;  // 8-bit inputs
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 
-template <int D, bool FP8>
+template <int D, bool QK8>
 struct FwdLayout {
-  static constexpr uint32_t QK_ELEM = FP8 ? 1 : 2;            // bytes per Q/K element
+  static constexpr uint32_t QK_ELEM = QK8 ? 1 : 2;            // bytes per Q/K element
   static constexpr uint32_t Q_BYTES = BM * D * QK_ELEM;
   static constexpr uint32_t K_BYTES = BN * D * QK_ELEM;
   static constexpr uint32_t V_BYTES = BN * D * 2;             // bf16 or f16
@@ -89,7 +89,8 @@ struct FwdParams {
   int nbatch;
   int n_loc;  // positions per sequence shard (n when unsharded)
   float scale_log2;
-  float o_scale;  // 8-bit inputs: 2^8 x the V scale, applied with 1/l
+  float o_scale;  // f16 P V: factor applied with 1/l (8-bit inputs: 2^8 x the V scale)
+  const float *v_inv;  // bf16 inputs with f16 P V: per K/V head 2^-k undoing V's scale
   __nv_bfloat16 *O;
   int64_t o_sbh, o_srow, o_sshard;
   float *LSE;
@@ -129,11 +130,18 @@ __device__ __forceinline__ int kv_tiles(const FwdParams &p, int nkb, int qb, int
   return last < nkb ? last : nkb;
 }
 
-template <int D, bool SHARDED, bool VARLEN, bool FP8>
+// MODE 0: bf16 Q, K, V; P V as the compensated bf16 pair.
+// MODE 1: bf16 Q, K; P V as one f16 product with V re-encoded in f16 (a
+//         per-head power-of-two scale, undone in the epilogue).
+// MODE 2: e4m3 Q, K (8-bit Q K^T); P V as in MODE 1 (V's codes times 2^-8).
+template <int D, bool SHARDED, bool VARLEN, int MODE>
 __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUtensorMap &tmK,
                                               const CUtensorMap &tmV, const FwdParams &p) {
-  static_assert(!FP8 || (D == 128 && !SHARDED && !VARLEN), "8-bit inputs: dense d = 128 only");
-  using L = FwdLayout<D, FP8>;
+  constexpr bool QK8 = MODE == 2;   // e4m3 Q, K
+  constexpr bool PV16 = MODE != 0;  // one f16 P V product
+  static_assert(!QK8 || D == 128, "8-bit inputs: d = 128 only");
+  static_assert(!PV16 || (!SHARDED && !VARLEN), "f16 P V: dense layouts only");
+  using L = FwdLayout<D, QK8>;
   // Q/K boxes: 128-byte rows of 64 bf16 or 128 e4m3 elements
   constexpr int QK_BOX = 128 / L::QK_ELEM;
   extern __shared__ uint8_t smem_raw[];
@@ -278,8 +286,8 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
     // The whole warp runs the loop; one elected lane issues each group of
     // products together with its commits.
     {
-      const uint32_t idS = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, 0, 0);
-      const uint32_t idO = FP8 ? idesc_f16_f32(BM, D, 0, 1) : idesc_bf16_f32(BM, D, 0, 1);
+      const uint32_t idS = QK8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, 0, 0);
+      const uint32_t idO = PV16 ? idesc_f16_f32(BM, D, 0, 1) : idesc_bf16_f32(BM, D, 0, 1);
       // Base descriptors built once; every MMA below only adds a
       // compile-time byte offset to the low word.
       const SDesc dQ0 = sdesc_make(smem_u32(smem + L::OFF_Q), 16, 1024);
@@ -297,7 +305,7 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
 #pragma unroll
         for (int kk = 0; kk < D * (int)L::QK_ELEM / 32; ++kk) {
           const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          if constexpr (FP8)
+          if constexpr (QK8)
             umma_f8_ss(tmem + t * BN, sdesc_at(a, off), sdesc_at(b, off), idS, kk > 0 ? 1u : 0u);
           else
             umma_f16_ss(tmem + t * BN, sdesc_at(a, off), sdesc_at(b, off), idS, kk > 0 ? 1u : 0u);
@@ -308,7 +316,7 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
       auto issue_pv = [&](int t, int j) {
         const SDesc b = (j & 1) ? dV1 : dV0;
         const uint32_t tP = tmem + t * BN;
-        if constexpr (FP8) {
+        if constexpr (PV16) {
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
             umma_f16_ts(tmem + 256 + t * 128, tP + kk * 8, sdesc_at(b, kk * 2048), idO,
@@ -419,10 +427,10 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
         }
       }
       // pass 1: row max, eight independent partial maxima (a tree, not a
-      // 128-long dependent chain); 8-bit inputs: four, two keys per
-      // three-input max
+      // 128-long dependent chain); f16 P V: four, two keys per three-input
+      // max
       float mx8[8];
-      if constexpr (FP8) {
+      if constexpr (PV16) {
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           mx8[u] = fmaxf(__uint_as_float(s[2 * u]), __uint_as_float(s[2 * u + 1]));
@@ -455,7 +463,7 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
       // over the columns already read: keys [16g, 16g+16) go to columns
       // [16g, 16g+8) (P_hi) and [16g+8, 16g+16) (P_lo), two keys per column.
       float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if constexpr (FP8) {
+      if constexpr (PV16) {
         // f16 P: keys [32g, 32g+32) to columns [16g, 16g+16); two keys per
         // packed fp32 instruction for x = s * scale - m and the row sum
         const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2);
@@ -483,7 +491,7 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
         }
       }
 #pragma unroll
-      for (int g = 0; g < (FP8 ? 0 : BN / 16); ++g) {
+      for (int g = 0; g < (PV16 ? 0 : BN / 16); ++g) {
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; k += 2) {
@@ -521,7 +529,8 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
     if (ok && mbar_wait(&pv_done[t], (nkv - 1) & 1, p.wc, abort_flag, SITE_FWD_EPI)) {
       tc_fence_after();
       float inv_l = 1.0f / l;
-      if constexpr (FP8) inv_l *= p.o_scale;
+      if constexpr (PV16) inv_l *= p.o_scale;
+      if constexpr (MODE == 1) inv_l *= __ldg(p.v_inv + bh / p.G);
       const int q_sh = SHARDED ? q_idx / p.n_loc : 0;
       __nv_bfloat16 *orow = p.O + (int64_t)bh * p.o_sbh + (int64_t)q_sh * p.o_sshard +
                             (int64_t)(row0 + q_idx - q_sh * p.n_loc) * p.o_srow;
@@ -547,7 +556,7 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
         p.LSE[(int64_t)bh * p.lse_sbh + row0 + q_idx] = (m + lg2(l)) * 0.69314718055994531f;
     }
   };
-  if constexpr (FP8) {
+  if constexpr (PV16) {
     if (warp >= 8) {  // warps 10 and 11 only hand their registers over
       setmaxnreg_dec<REGS_CONTROL>();
       if (warp == 8)
@@ -580,7 +589,7 @@ __global__ void __launch_bounds__(fwd_threads<false>(), 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  attn_fwd_body<D, SHARDED, VARLEN, false>(tmQ, tmK, tmV, p);
+  attn_fwd_body<D, SHARDED, VARLEN, 0>(tmQ, tmK, tmV, p);
 }
 
 template <int D>
@@ -588,7 +597,15 @@ __global__ void __launch_bounds__(fwd_threads<true>(), 1)
     attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  attn_fwd_body<D, false, false, true>(tmQ, tmK, tmV, p);
+  attn_fwd_body<D, false, false, 2>(tmQ, tmK, tmV, p);
+}
+
+template <int D>
+__global__ void __launch_bounds__(fwd_threads<true>(), 1)
+    attn_fwd_pv16_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  attn_fwd_body<D, false, false, 1>(tmQ, tmK, tmV, p);
 }
 
 // e4m3 V [BHkv][n][128] (strided rows) -> f16 [BHkv][n][128] packed, each
@@ -620,6 +637,81 @@ __global__ void __launch_bounds__(256)
     uint4 *dst = reinterpret_cast<uint4 *>(out + r * 128 + c * 16);
     dst[0] = make_uint4(y[0], y[1], y[2], y[3]);
     dst[1] = make_uint4(y[4], y[5], y[6], y[7]);
+  }
+}
+
+// bf16 V -> f16 with one power-of-two scale 2^k per K/V head, chosen from the
+// head's largest |v| so that it lands in [2^14, 2^15): every value keeps its
+// 8 significant bits in f16 exactly, except values smaller than 2^-31 of
+// that maximum, which fall into f16's subnormal range and are rounded with an
+// absolute error of at most 2^-39 of the maximum.  Two passes over V in row chunks of VCH_ROWS rows:
+// v_absmax_kernel writes each chunk's largest |v| (as bf16 magnitude bits,
+// which order like the values), v_to_f16_kernel reduces a head's chunk
+// maxima, converts its chunk and (chunk 0) stores 2^-k for the epilogue.
+constexpr int VCH_ROWS = 256;
+
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = red[0];
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) v = max(v, red[w]);
+  __syncthreads();
+  return v;
+}
+
+template <int D>
+__global__ void __launch_bounds__(256)
+    v_absmax_kernel(const __nv_bfloat16 *__restrict__ V, int64_t s_bh, int64_t s_row, int n,
+                    int nch, uint32_t *__restrict__ part) {
+  __shared__ uint32_t red[8];
+  const int h = blockIdx.y, ch = blockIdx.x;
+  const int r0 = ch * VCH_ROWS;
+  const int rows = min(VCH_ROWS, n - r0);
+  constexpr int VPR = D / 8;  // 16-byte vectors per row
+  uint32_t m = 0;
+  for (int i = threadIdx.x; i < rows * VPR; i += blockDim.x) {
+    const int r = i / VPR, c = i % VPR;
+    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(V + h * s_bh + (int64_t)(r0 + r) * s_row) + c);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7fffu, (w[k] >> 16) & 0x7fffu));
+  }
+  m = block_max_u32(m, red);
+  if (threadIdx.x == 0) part[(int64_t)h * nch + ch] = m;
+}
+
+template <int D>
+__global__ void __launch_bounds__(256)
+    v_to_f16_kernel(const __nv_bfloat16 *__restrict__ V, int64_t s_bh, int64_t s_row, int n,
+                    int nch, const uint32_t *__restrict__ part, uint16_t *__restrict__ out,
+                    float *__restrict__ v_inv) {
+  __shared__ uint32_t red[8];
+  const int h = blockIdx.y, ch = blockIdx.x;
+  uint32_t m = 0;
+  for (int i = threadIdx.x; i < nch; i += blockDim.x) m = max(m, part[(int64_t)h * nch + i]);
+  m = block_max_u32(m, red);
+  // m: bf16 bits of the head's largest |v|; its exponent field e gives
+  // |v|max in [2^(e-127), 2^(e-126)), so k = 141 - e puts it in [2^14, 2^15).
+  // Zero, infinite or NaN maxima keep k = 0.
+  const int e = (int)(m >> 7);
+  int k = (m == 0 || e == 255) ? 0 : 141 - e;
+  k = k < -126 ? -126 : (k > 126 ? 126 : k);
+  const float sc = __uint_as_float((uint32_t)(127 + k) << 23);
+  if (ch == 0 && threadIdx.x == 0) v_inv[h] = __uint_as_float((uint32_t)(127 - k) << 23);
+  const int r0 = ch * VCH_ROWS;
+  const int rows = min(VCH_ROWS, n - r0);
+  constexpr int VPR = D / 8;
+  for (int i = threadIdx.x; i < rows * VPR; i += blockDim.x) {
+    const int r = i / VPR, c = i % VPR;
+    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(V + h * s_bh + (int64_t)(r0 + r) * s_row) + c);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t y[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      y[q] = pack_f16(__uint_as_float(w[q] << 16) * sc, __uint_as_float(w[q] & 0xffff0000u) * sc);
+    reinterpret_cast<uint4 *>(out + ((int64_t)h * n + r0 + r) * D)[c] = make_uint4(y[0], y[1], y[2], y[3]);
   }
 }
 
@@ -664,6 +756,7 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t s
   p.causal = a.causal;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.o_scale = 1.0f;
+  p.v_inv = nullptr;
   p.O = static_cast<__nv_bfloat16 *>(a.O);
   p.o_sbh = a.o_sbh;
   p.o_srow = a.o_srow;
@@ -731,6 +824,7 @@ cudaError_t launch_attn_fwd_fp8(const AttnFwdArgs &a, void *v16, const WaitCfg &
   p.causal = a.causal;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.o_scale = 256.0f * a.v_scale;
+  p.v_inv = nullptr;
   p.O = static_cast<__nv_bfloat16 *>(a.O);
   p.o_sbh = a.o_sbh;
   p.o_srow = a.o_srow;
@@ -748,6 +842,80 @@ cudaError_t launch_attn_fwd_fp8(const AttnFwdArgs &a, void *v16, const WaitCfg &
       <<<(unsigned)(p.nqb2 * a.BH), fwd_threads<true>(), L::ALLOC, st>>>(mq, mk, mv, p);
   timing_mark(st, 2);
   return cudaGetLastError();
+}
+
+size_t attn_fwd_pv16_workspace(int BHkv, int n, int d) {
+  const size_t vb = ((size_t)2 * BHkv * n * d + 255) & ~(size_t)255;
+  const size_t nch = (size_t)(n + VCH_ROWS - 1) / VCH_ROWS;
+  return vb + ((4 * (size_t)BHkv * nch + 255) & ~(size_t)255) + ((4 * (size_t)BHkv + 255) & ~(size_t)255);
+}
+
+template <int D>
+static cudaError_t launch_pv16_d(const AttnFwdArgs &a, void *ws, const WaitCfg &wc,
+                                 cudaStream_t st) {
+  using L = FwdLayout<D, false>;
+  const int nch = (a.n + VCH_ROWS - 1) / VCH_ROWS;
+  uint8_t *base = static_cast<uint8_t *>(ws);
+  const size_t vb = ((size_t)2 * a.BHkv * a.n * D + 255) & ~(size_t)255;
+  uint16_t *v16 = reinterpret_cast<uint16_t *>(base);
+  uint32_t *part = reinterpret_cast<uint32_t *>(base + vb);
+  float *v_inv = reinterpret_cast<float *>(base + vb + ((4 * (size_t)a.BHkv * nch + 255) & ~(size_t)255));
+  const dim3 vgrid((unsigned)nch, (unsigned)a.BHkv);
+  const __nv_bfloat16 *V = static_cast<const __nv_bfloat16 *>(a.V);
+  timing_mark(st, 0);
+  v_absmax_kernel<D><<<vgrid, 256, 0, st>>>(V, a.v_sbh, a.v_srow, a.n, nch, part);
+  v_to_f16_kernel<D><<<vgrid, 256, 0, st>>>(V, a.v_sbh, a.v_srow, a.n, nch, part, v16, v_inv);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mq, mk, mv;
+  const uint32_t box[3] = {64, 128, 1};
+  const uint64_t dq[3] = {(uint64_t)D, (uint64_t)a.n, (uint64_t)a.BH};
+  const uint64_t dkv[3] = {(uint64_t)D, (uint64_t)a.n, (uint64_t)a.BHkv};
+  const uint64_t sq[2] = {(uint64_t)a.q_srow * 2, (uint64_t)a.q_sbh * 2};
+  const uint64_t sk[2] = {(uint64_t)a.k_srow * 2, (uint64_t)a.k_sbh * 2};
+  const uint64_t sv[2] = {(uint64_t)D * 2, (uint64_t)a.n * D * 2};
+  if ((e = make_tmap(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.Q, dq, sq, box)) != cudaSuccess)
+    return e;
+  if ((e = make_tmap(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.K, dkv, sk, box)) != cudaSuccess)
+    return e;
+  if ((e = make_tmap(&mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, v16, dkv, sv, box)) != cudaSuccess)
+    return e;
+  FwdParams p;
+  p.BH = a.BH;
+  p.n = a.n;
+  p.cu = nullptr;
+  p.nbatch = 0;
+  p.nqb2 = (a.n + 2 * BM - 1) / (2 * BM);
+  p.nkb = (a.n + BN - 1) / BN;
+  p.causal = a.causal;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.o_scale = 1.0f;
+  p.v_inv = v_inv;
+  p.O = static_cast<__nv_bfloat16 *>(a.O);
+  p.o_sbh = a.o_sbh;
+  p.o_srow = a.o_srow;
+  p.o_sshard = 0;
+  p.n_loc = a.n;
+  p.G = a.BH / a.BHkv;
+  p.LSE = a.LSE;
+  p.lse_sbh = a.lse_sbh;
+  p.wc = wc;
+  e = cudaFuncSetAttribute(attn_fwd_pv16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           L::ALLOC);
+  if (e != cudaSuccess) return e;
+  timing_mark(st, 1);
+  attn_fwd_pv16_kernel<D>
+      <<<(unsigned)(p.nqb2 * a.BH), fwd_threads<true>(), L::ALLOC, st>>>(mq, mk, mv, p);
+  timing_mark(st, 2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_fwd_pv16(const AttnFwdArgs &a, void *ws, const WaitCfg &wc,
+                                 cudaStream_t st) {
+  if (a.n_loc != a.n || a.cu_seqlens) return cudaErrorNotSupported;
+  if (a.d == 128) return launch_pv16_d<128>(a, ws, wc, st);
+  if (a.d == 64) return launch_pv16_d<64>(a, ws, wc, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace chain

@@ -643,6 +643,57 @@ int chain_bwd_varlen(const chain_tensor_t *dO, const chain_tensor_t *Q, const ch
   return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
 }
 
+size_t chain_fwd_f16pv_workspace_size(const chain_tensor_t *Q, const chain_tensor_t *V) {
+  View q, v;
+  if (view_of(Q, 2, &q) || view_of(V, 2, &v) || !kv_shape(q, v)) return 0;
+  if (q.rows < 1 || q.rows > (1 << 30) || v.outer < 1 || v.outer > 65535 * 16) return 0;
+  return attn_fwd_pv16_workspace((int)v.outer, (int)v.rows, (int)v.cols);
+}
+
+int chain_fwd_f16pv(const chain_tensor_t *Q, const chain_tensor_t *K, const chain_tensor_t *V,
+                    int mask, float scale, chain_tensor_t *O, chain_tensor_t *LSE,
+                    void *workspace, size_t ws_bytes, void *stream) {
+  if (mask != CHAIN_MASK_NONE && mask != CHAIN_MASK_CAUSAL) return CHAIN_ERR_ARG;
+  View q, k, v, o;
+  int rc;
+  if ((rc = view_of(Q, 2, &q)) || (rc = view_of(K, 2, &k)) || (rc = view_of(V, 2, &v)) ||
+      (rc = view_of(O, 2, &o)))
+    return rc;
+  if (q.dtype != CHAIN_BF16 || k.dtype != CHAIN_BF16 || v.dtype != CHAIN_BF16 ||
+      o.dtype != CHAIN_BF16)
+    return CHAIN_ERR_DTYPE;
+  if (!kv_shape(q, k) || !same_shape(k, v) || !same_shape(q, o)) return CHAIN_ERR_ARG;
+  if (q.cols != 64 && q.cols != 128) return CHAIN_ERR_ARG;
+  if (q.rows < 1 || q.outer < 1) return CHAIN_ERR_ARG;
+  if (q.rows > (1 << 30) || q.outer > 65535 * 16) return CHAIN_ERR_ARG;
+  if (!(scale > 0.0f) || !(scale < 1e30f)) return CHAIN_ERR_ARG;
+  if (!pitch16(q) || !pitch16(k) || !pitch16(v) || !pitch16(o)) return CHAIN_ERR_ARG;
+  int64_t lse_sbh = 0;
+  if ((rc = lse_view(LSE, q.outer, q.rows, &lse_sbh))) return rc;
+  if (!workspace || !aligned16(workspace) ||
+      ws_bytes < attn_fwd_pv16_workspace((int)v.outer, (int)v.rows, (int)v.cols))
+    return CHAIN_ERR_ARG;
+  AttnFwdArgs args;
+  args.Q = q.ptr; args.K = k.ptr; args.V = v.ptr;
+  args.q_sbh = q.s_outer; args.q_srow = q.s_row;
+  args.k_sbh = k.s_outer; args.k_srow = k.s_row;
+  args.v_sbh = v.s_outer; args.v_srow = v.s_row;
+  args.O = o.ptr; args.o_sbh = o.s_outer; args.o_srow = o.s_row;
+  args.LSE = static_cast<float *>(LSE->ptr); args.lse_sbh = lse_sbh;
+  args.BH = (int)q.outer; args.n = (int)q.rows; args.d = (int)q.cols;
+  args.BHkv = (int)k.outer;
+  args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
+  args.n_loc = args.n;
+  args.q_sshard = args.k_sshard = args.v_sshard = args.o_sshard = 0;
+  args.cu_seqlens = nullptr; args.nbatch = 0; args.max_seqlen = 0;
+  DevInfo *di = nullptr;
+  if ((rc = device_ready(&di))) return rc;
+  cudaError_t e = launch_attn_fwd_pv16(args, workspace, wait_cfg(di),
+                                       static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return CHAIN_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
+}
+
 static size_t fp8_ws_bytes(const View &v) {
   return ((size_t)(v.outer * v.rows * v.cols * 2) + 255) & ~(size_t)255;
 }

@@ -41,6 +41,12 @@ cudaError_t launch_attn_fwd_bf16(const AttnFwdArgs &a, const WaitCfg &wc, cudaSt
 // (16-byte aligned) for the f16 copy of V.
 cudaError_t launch_attn_fwd_fp8(const AttnFwdArgs &a, void *v16, const WaitCfg &wc,
                                cudaStream_t st);
+// bf16 Q, K, V with P V as one f16 product (V re-encoded in f16 with a
+// power-of-two scale per K/V head); ws = attn_fwd_pv16_workspace bytes,
+// 16-byte aligned.  Dense layouts, d = 64 or 128.
+size_t attn_fwd_pv16_workspace(int BHkv, int n, int d);
+cudaError_t launch_attn_fwd_pv16(const AttnFwdArgs &a, void *ws, const WaitCfg &wc,
+                                 cudaStream_t st);
 cudaError_t launch_attn_fwd_f32(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t st);
 
 struct AttnBwdArgs {

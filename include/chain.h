@@ -272,6 +272,33 @@ int chain_bwd_varlen(const chain_tensor_t *dO, const chain_tensor_t *Q,
                      chain_tensor_t *dV, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * chain_fwd_f16pv -- softmax attention forward, the same operation as
+ * chain_fwd with f = CHAIN_F_SOFTMAX on bf16 inputs (the unit O = f(A B) C
+ * of "Memory-efficient tensor parallelism", FITEE 10.1631/FITEE.2400602,
+ * abstract, tiled as in "Ulysses Sequence Parallelism", "Contexte
+ * Technique"), with the second product P V taken as ONE f16 tensor-core
+ * product instead of chain_fwd's compensated bf16 pair: P enters as f16 (11
+ * significant bits) and V as an f16 copy in the caller's workspace.
+ *   Q [BH][n][d], K, V [BHkv][n][d] bf16 (BHkv dividing BH), O [BH][n][d]
+ *   bf16, LSE [BH][n] fp32; d = 64 or 128; 3-D or 4-D (B*H folded); row and
+ *   head pitches multiples of 16 bytes.  mask, scale as for chain_fwd.
+ *   workspace  at least chain_fwd_f16pv_workspace_size(Q, V) bytes, 16-byte
+ *              aligned: V in f16 (2 * BHkv * n * d bytes) and per-head
+ *              scale factors.
+ * The copy of V carries one power-of-two scale per K/V head that puts the
+ * head's largest |v| in [2^14, 2^15); every value is then exact in f16 except
+ * values below 2^-31 of that maximum, rounded with an error of at most 2^-39
+ * of it.  The epilogue undoes the scale.  Error: one bf16 rounding of O plus
+ * P's f16 rounding (~2^-12 relative, random over the keys).  Returns
+ * CHAIN_ERR_DTYPE unless bf16, CHAIN_ERR_ARG for a shape, stride, alignment
+ * or workspace violation.  Asynchronous on `stream`.
+ */
+size_t chain_fwd_f16pv_workspace_size(const chain_tensor_t *Q, const chain_tensor_t *V);
+int chain_fwd_f16pv(const chain_tensor_t *Q, const chain_tensor_t *K,
+                    const chain_tensor_t *V, int mask, float scale, chain_tensor_t *O,
+                    chain_tensor_t *LSE, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * chain_fwd_fp8 -- softmax attention, O = softmax(scale Q K^T) (v_scale V),
  * on 8-bit float inputs: the unit O = f(A B) C of "Memory-efficient tensor
  * parallelism" (FITEE 10.1631/FITEE.2400602, abstract) with f = row softmax,
