@@ -759,8 +759,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(s_free);  // S(j+1) may overwrite these columns
+        // two keys per packed fp32 fma
+        const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2);
+        const uint64_t nl2 = f32x2(-lse2, -lse2);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pf[c] = ex2(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lse2));
+        for (int c = 0; c < 64; c += 2) {
+          float a0, a1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl2),
+                      a0, a1);
+          pf[c] = ex2(a0);
+          pf[c + 1] = ex2(a1);
+        }
         // keys after the query (diagonal tile) or beyond n (ragged tile): one
         // branch around the whole pass, none in the loop above
         if (masked) {
@@ -782,10 +791,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_ld32(tdP + lane_off + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
         tmem_wait_ld();
         uint32_t ds[32];
+        const uint64_t dv2 = f32x2(dval, dval);
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          ds[c] = pack_bf16(pf[2 * c] * (__uint_as_float(dp[2 * c]) - dval),
-                            pf[2 * c + 1] * (__uint_as_float(dp[2 * c + 1]) - dval));
+        for (int c = 0; c < 32; ++c) {
+          float a0, a1;
+          f32x2_split(mul_f32x2(f32x2(pf[2 * c], pf[2 * c + 1]),
+                                sub_f32x2(f32x2(__uint_as_float(dp[2 * c]),
+                                                __uint_as_float(dp[2 * c + 1])), dv2)),
+                      a0, a1);
+          ds[c] = pack_bf16(a0, a1);
+        }
         // dS over the first half of the dP columns this warpgroup just read
         tmem_st32(tdP + lane_off + 64 * w, ds);
       }
