@@ -79,6 +79,10 @@ def _load():
             lib.chain_fwd_fp8.argtypes = [P, P, P, ci, fl, fl, P, P, vp, ctypes.c_size_t, vp]
             lib.chain_fwd_f16pv.argtypes = [P, P, P, ci, fl, P, P, vp, ctypes.c_size_t, vp]
             lib.chain_fwd_f16pv_workspace_size.argtypes = [P, P]
+            lib.chain_fwd_sp_f16pv.argtypes = [P, P, P, ci, ci, ci, fl, P, P, vp, ctypes.c_size_t,
+                                               vp]
+            lib.chain_fwd_sp_f16pv_workspace_size.argtypes = [P, ci]
+            lib.chain_fwd_sp_f16pv_workspace_size.restype = ctypes.c_size_t
             lib.chain_fwd_f16pv_workspace_size.restype = ctypes.c_size_t
             lib.chain_fwd_fp8_workspace_size.argtypes = [P]
             lib.chain_fwd_fp8_workspace_size.restype = ctypes.c_size_t
@@ -95,6 +99,7 @@ def _load():
             lib.chain_status_string.restype = ctypes.c_char_p
             for fn in ("chain_fwd", "chain_fwd_sp", "chain_fwd_varlen", "chain_bwd", "chain_bwd_varlen",
                        "chain_bwd_noalloc", "chain_fwd_fp8", "chain_fwd_f16pv",
+                       "chain_fwd_sp_f16pv",
                        "sp_relayout",
                        "sp_relayout_inverse",
                        "chain_check", "chain_selftest_wait_timeout", "chain_umma_selftest",
@@ -180,6 +185,19 @@ def chain_fwd_f16pv(Q, K, V, mask, scale, O, LSE, workspace, stream=None):
                                 ctypes.c_void_p(workspace.data_ptr()),
                                 workspace.numel() * workspace.element_size(), _stream(stream)),
         "chain_fwd_f16pv")
+
+
+def chain_fwd_sp_f16pv(Q, K, V, p, head_group, mask, scale, O, LSE, workspace, stream=None):
+    """chain_fwd_sp with P V as one f16 product; see include/chain.h."""
+    _ok(_load().chain_fwd_sp_f16pv(_ref(desc(Q)), _ref(desc(K)), _ref(desc(V)), int(p),
+                                   int(head_group), int(mask), float(scale), _ref(desc(O)),
+                                   _ref(desc(LSE)), ctypes.c_void_p(workspace.data_ptr()),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+        "chain_fwd_sp_f16pv")
+
+
+def chain_fwd_sp_f16pv_workspace_size(V, p) -> int:
+    return int(_load().chain_fwd_sp_f16pv_workspace_size(_ref(desc(V)), int(p)))
 
 
 def chain_fwd_f16pv_workspace_size(Q, V) -> int:
@@ -340,6 +358,22 @@ def attention_fwd_sp(q, k, v, p: int, head_group: int, causal: bool, scale: floa
         o = torch.zeros_like(q)
     lse = torch.empty(H // p, p * n_loc, dtype=torch.float32, device=q.device)
     chain_fwd_sp(q, k, v, p, head_group, MASK_CAUSAL if causal else MASK_NONE, scale, o, lse, stream)
+    return o, lse
+
+
+def attention_fwd_sp_f16pv(q, k, v, p: int, head_group: int, causal: bool,
+                           scale: float | None = None, o=None, workspace=None, stream=None):
+    """attention_fwd_sp with P V as one f16 product."""
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    P, n_loc, H, d = q.shape
+    if o is None:
+        o = torch.zeros_like(q)
+    lse = torch.empty(H // p, p * n_loc, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(max(chain_fwd_sp_f16pv_workspace_size(v, p), 16),
+                                dtype=torch.uint8, device=q.device)
+    chain_fwd_sp_f16pv(q, k, v, p, head_group, MASK_CAUSAL if causal else MASK_NONE, scale, o, lse,
+                       workspace, stream)
     return o, lse
 
 

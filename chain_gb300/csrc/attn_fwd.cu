@@ -140,7 +140,8 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
   constexpr bool QK8 = MODE == 2;   // e4m3 Q, K
   constexpr bool PV16 = MODE != 0;  // one f16 P V product
   static_assert(!QK8 || D == 128, "8-bit inputs: d = 128 only");
-  static_assert(!PV16 || (!SHARDED && !VARLEN), "f16 P V: dense layouts only");
+  static_assert(!PV16 || !VARLEN, "f16 P V: no packed sequences");
+  static_assert(!QK8 || !SHARDED, "8-bit inputs: head-major layout only");
   using L = FwdLayout<D, QK8>;
   // Q/K boxes: 128-byte rows of 64 bf16 or 128 e4m3 elements
   constexpr int QK_BOX = 128 / L::QK_ELEM;
@@ -265,9 +266,13 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
           break;
         mbar_arrive_expect_tx(&v_full[st], L::V_BYTES);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          load(smem + L::OFF_V + st * L::V_BYTES + c * (BN * 128), &tmV, &v_full[st], c * 64,
-               j * BN, bkv);
+        for (int c = 0; c < D / 64; ++c) {
+          uint8_t *dst = smem + L::OFF_V + st * L::V_BYTES + c * (BN * 128);
+          if constexpr (PV16)  // the f16 copy of V is head-major in every layout
+            tma_load_3d(dst, &tmV, &v_full[st], c * 64, j * BN, bkv);
+          else
+            load(dst, &tmV, &v_full[st], c * 64, j * BN, bkv);
+        }
         v_issued = j + 1;
       }
       if (*abort_flag) {
@@ -608,6 +613,16 @@ __global__ void __launch_bounds__(fwd_threads<true>(), 1)
   attn_fwd_body<D, false, false, 1>(tmQ, tmK, tmV, p);
 }
 
+// The same over Ulysses sequence shards: Q, K read from and O written to
+// [p][n_loc][H][d]; V's f16 copy is head-major (its pre-pass reads the shards).
+template <int D>
+__global__ void __launch_bounds__(fwd_threads<true>(), 1)
+    attn_fwd_sp_pv16_kernel(const __grid_constant__ CUtensorMap tmQ,
+                            const __grid_constant__ CUtensorMap tmK,
+                            const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  attn_fwd_body<D, true, false, 1>(tmQ, tmK, tmV, p);
+}
+
 // e4m3 V [BHkv][n][128] (strided rows) -> f16 [BHkv][n][128] packed, each
 // value times 2^-8, exactly.  An e4m3 byte s.eeee.mmm placed as the f16 bit
 // pattern s.0eeee.mmm0000000 is the same number scaled by 2^(7-15): the f16
@@ -661,10 +676,19 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red) {
   return v;
 }
 
+// Row t of head h lives at V + h s_bh + (t / n_loc) s_shard + (t % n_loc) s_row
+// (n_loc = n, s_shard = 0 for one contiguous sequence).
+__device__ __forceinline__ const __nv_bfloat16 *v_row(const __nv_bfloat16 *V, int64_t s_bh,
+                                                      int64_t s_row, int64_t s_shard, int n_loc,
+                                                      int h, int t) {
+  const int sh = t / n_loc;
+  return V + h * s_bh + sh * s_shard + (int64_t)(t - sh * n_loc) * s_row;
+}
+
 template <int D>
 __global__ void __launch_bounds__(256)
-    v_absmax_kernel(const __nv_bfloat16 *__restrict__ V, int64_t s_bh, int64_t s_row, int n,
-                    int nch, uint32_t *__restrict__ part) {
+    v_absmax_kernel(const __nv_bfloat16 *__restrict__ V, int64_t s_bh, int64_t s_row,
+                    int64_t s_shard, int n_loc, int n, int nch, uint32_t *__restrict__ part) {
   __shared__ uint32_t red[8];
   const int h = blockIdx.y, ch = blockIdx.x;
   const int r0 = ch * VCH_ROWS;
@@ -673,7 +697,8 @@ __global__ void __launch_bounds__(256)
   uint32_t m = 0;
   for (int i = threadIdx.x; i < rows * VPR; i += blockDim.x) {
     const int r = i / VPR, c = i % VPR;
-    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(V + h * s_bh + (int64_t)(r0 + r) * s_row) + c);
+    const uint4 x =
+        __ldg(reinterpret_cast<const uint4 *>(v_row(V, s_bh, s_row, s_shard, n_loc, h, r0 + r)) + c);
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7fffu, (w[k] >> 16) & 0x7fffu));
@@ -684,8 +709,9 @@ __global__ void __launch_bounds__(256)
 
 template <int D>
 __global__ void __launch_bounds__(256)
-    v_to_f16_kernel(const __nv_bfloat16 *__restrict__ V, int64_t s_bh, int64_t s_row, int n,
-                    int nch, const uint32_t *__restrict__ part, uint16_t *__restrict__ out,
+    v_to_f16_kernel(const __nv_bfloat16 *__restrict__ V, int64_t s_bh, int64_t s_row,
+                    int64_t s_shard, int n_loc, int n, int nch,
+                    const uint32_t *__restrict__ part, uint16_t *__restrict__ out,
                     float *__restrict__ v_inv) {
   __shared__ uint32_t red[8];
   const int h = blockIdx.y, ch = blockIdx.x;
@@ -705,7 +731,8 @@ __global__ void __launch_bounds__(256)
   constexpr int VPR = D / 8;
   for (int i = threadIdx.x; i < rows * VPR; i += blockDim.x) {
     const int r = i / VPR, c = i % VPR;
-    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(V + h * s_bh + (int64_t)(r0 + r) * s_row) + c);
+    const uint4 x =
+        __ldg(reinterpret_cast<const uint4 *>(v_row(V, s_bh, s_row, s_shard, n_loc, h, r0 + r)) + c);
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
     uint32_t y[4];
 #pragma unroll
@@ -862,23 +889,38 @@ static cudaError_t launch_pv16_d(const AttnFwdArgs &a, void *ws, const WaitCfg &
   float *v_inv = reinterpret_cast<float *>(base + vb + ((4 * (size_t)a.BHkv * nch + 255) & ~(size_t)255));
   const dim3 vgrid((unsigned)nch, (unsigned)a.BHkv);
   const __nv_bfloat16 *V = static_cast<const __nv_bfloat16 *>(a.V);
+  const bool sharded = a.n_loc != a.n;
+  const int64_t v_sshard = sharded ? a.v_sshard : 0;
   timing_mark(st, 0);
-  v_absmax_kernel<D><<<vgrid, 256, 0, st>>>(V, a.v_sbh, a.v_srow, a.n, nch, part);
-  v_to_f16_kernel<D><<<vgrid, 256, 0, st>>>(V, a.v_sbh, a.v_srow, a.n, nch, part, v16, v_inv);
+  v_absmax_kernel<D><<<vgrid, 256, 0, st>>>(V, a.v_sbh, a.v_srow, v_sshard, a.n_loc, a.n, nch,
+                                            part);
+  v_to_f16_kernel<D><<<vgrid, 256, 0, st>>>(V, a.v_sbh, a.v_srow, v_sshard, a.n_loc, a.n, nch,
+                                            part, v16, v_inv);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  // Q, K: {d, row, head}, or {d, row in shard, shard, head} over sequence
+  // shards; V's f16 copy: {d, row, head}
   CUtensorMap mq, mk, mv;
-  const uint32_t box[3] = {64, 128, 1};
-  const uint64_t dq[3] = {(uint64_t)D, (uint64_t)a.n, (uint64_t)a.BH};
-  const uint64_t dkv[3] = {(uint64_t)D, (uint64_t)a.n, (uint64_t)a.BHkv};
-  const uint64_t sq[2] = {(uint64_t)a.q_srow * 2, (uint64_t)a.q_sbh * 2};
-  const uint64_t sk[2] = {(uint64_t)a.k_srow * 2, (uint64_t)a.k_sbh * 2};
+  const int rank = sharded ? 4 : 3;
+  const uint32_t box[4] = {64, 128, 1, 1};
+  const int64_t nsh = a.n / a.n_loc;
+  uint64_t dq[4] = {(uint64_t)D, (uint64_t)a.n_loc, (uint64_t)nsh, (uint64_t)a.BH};
+  uint64_t dk[4] = {(uint64_t)D, (uint64_t)a.n_loc, (uint64_t)nsh, (uint64_t)a.BHkv};
+  uint64_t sq[3] = {(uint64_t)a.q_srow * 2, (uint64_t)a.q_sshard * 2, (uint64_t)a.q_sbh * 2};
+  uint64_t sk[3] = {(uint64_t)a.k_srow * 2, (uint64_t)a.k_sshard * 2, (uint64_t)a.k_sbh * 2};
+  if (!sharded) {  // drop the shard dimension
+    dq[2] = dq[3];
+    dk[2] = dk[3];
+    sq[1] = sq[2];
+    sk[1] = sk[2];
+  }
+  const uint64_t dv[3] = {(uint64_t)D, (uint64_t)a.n, (uint64_t)a.BHkv};
   const uint64_t sv[2] = {(uint64_t)D * 2, (uint64_t)a.n * D * 2};
-  if ((e = make_tmap(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.Q, dq, sq, box)) != cudaSuccess)
+  if ((e = make_tmap(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, a.Q, dq, sq, box)) != cudaSuccess)
     return e;
-  if ((e = make_tmap(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.K, dkv, sk, box)) != cudaSuccess)
+  if ((e = make_tmap(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, a.K, dk, sk, box)) != cudaSuccess)
     return e;
-  if ((e = make_tmap(&mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, v16, dkv, sv, box)) != cudaSuccess)
+  if ((e = make_tmap(&mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, v16, dv, sv, box)) != cudaSuccess)
     return e;
   FwdParams p;
   p.BH = a.BH;
@@ -894,25 +936,24 @@ static cudaError_t launch_pv16_d(const AttnFwdArgs &a, void *ws, const WaitCfg &
   p.O = static_cast<__nv_bfloat16 *>(a.O);
   p.o_sbh = a.o_sbh;
   p.o_srow = a.o_srow;
-  p.o_sshard = 0;
-  p.n_loc = a.n;
+  p.o_sshard = sharded ? a.o_sshard : 0;
+  p.n_loc = a.n_loc;
   p.G = a.BH / a.BHkv;
   p.LSE = a.LSE;
   p.lse_sbh = a.lse_sbh;
   p.wc = wc;
-  e = cudaFuncSetAttribute(attn_fwd_pv16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           L::ALLOC);
+  auto kern = sharded ? attn_fwd_sp_pv16_kernel<D> : attn_fwd_pv16_kernel<D>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   timing_mark(st, 1);
-  attn_fwd_pv16_kernel<D>
-      <<<(unsigned)(p.nqb2 * a.BH), fwd_threads<true>(), L::ALLOC, st>>>(mq, mk, mv, p);
+  kern<<<(unsigned)(p.nqb2 * a.BH), fwd_threads<true>(), L::ALLOC, st>>>(mq, mk, mv, p);
   timing_mark(st, 2);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attn_fwd_pv16(const AttnFwdArgs &a, void *ws, const WaitCfg &wc,
                                  cudaStream_t st) {
-  if (a.n_loc != a.n || a.cu_seqlens) return cudaErrorNotSupported;
+  if (a.cu_seqlens) return cudaErrorNotSupported;
   if (a.d == 128) return launch_pv16_d<128>(a, ws, wc, st);
   if (a.d == 64) return launch_pv16_d<64>(a, ws, wc, st);
   return cudaErrorInvalidValue;

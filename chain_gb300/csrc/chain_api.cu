@@ -553,6 +553,57 @@ int chain_fwd_sp(const chain_tensor_t *Q, const chain_tensor_t *K, const chain_t
   return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
 }
 
+size_t chain_fwd_sp_f16pv_workspace_size(const chain_tensor_t *V, int p) {
+  if (!V || V->ndim != 4 || p <= 0 || V->shape[0] != p || V->shape[2] % p) return 0;
+  const int64_t n = p * V->shape[1], Hl = V->shape[2] / p, d = V->shape[3];
+  if (n <= 0 || n > (1 << 30) || Hl <= 0 || Hl > 65535 * 16 || (d != 64 && d != 128)) return 0;
+  return attn_fwd_pv16_workspace((int)Hl, (int)n, (int)d);
+}
+
+int chain_fwd_sp_f16pv(const chain_tensor_t *Q, const chain_tensor_t *K, const chain_tensor_t *V,
+                       int p, int head_group, int mask, float scale, chain_tensor_t *O,
+                       chain_tensor_t *LSE, void *workspace, size_t ws_bytes, void *stream) {
+  if (!Q || Q->ndim != 4) return CHAIN_ERR_ARG;
+  if (mask != CHAIN_MASK_NONE && mask != CHAIN_MASK_CAUSAL) return CHAIN_ERR_ARG;
+  if (p <= 0 || head_group < 0 || head_group >= p) return CHAIN_ERR_ARG;
+  const int64_t n_loc = Q->shape[1], H = Q->shape[2], d = Q->shape[3];
+  int rc;
+  if ((rc = shard_view(Q, p, n_loc, H, d)) || (rc = shard_view(K, p, n_loc, H, d)) ||
+      (rc = shard_view(V, p, n_loc, H, d)) || (rc = shard_view(O, p, n_loc, H, d)))
+    return rc;
+  if (n_loc <= 0 || H <= 0 || H % p || (d != 64 && d != 128)) return CHAIN_ERR_ARG;
+  if (!(scale > 0.0f) || !(scale < 1e30f)) return CHAIN_ERR_ARG;
+  const int64_t Hl = H / p, n = p * n_loc;
+  if (n > (1 << 30) || Hl > 65535 * 16) return CHAIN_ERR_ARG;
+  if (n_loc % 128) return CHAIN_ERR_UNSUPPORTED;  // a 128-row tile must not cross shards
+  int64_t lse_sbh = 0;
+  if ((rc = lse_view(LSE, Hl, n, &lse_sbh))) return rc;
+  if (!workspace || !aligned16(workspace) ||
+      ws_bytes < attn_fwd_pv16_workspace((int)Hl, (int)n, (int)d))
+    return CHAIN_ERR_ARG;
+  const int64_t h0 = (int64_t)head_group * Hl;
+  AttnFwdArgs args;
+  args.Q = static_cast<const __nv_bfloat16 *>(Q->ptr) + h0 * Q->stride[2];
+  args.K = static_cast<const __nv_bfloat16 *>(K->ptr) + h0 * K->stride[2];
+  args.V = static_cast<const __nv_bfloat16 *>(V->ptr) + h0 * V->stride[2];
+  args.O = static_cast<__nv_bfloat16 *>(O->ptr) + h0 * O->stride[2];
+  args.q_sbh = Q->stride[2]; args.q_srow = Q->stride[1]; args.q_sshard = Q->stride[0];
+  args.k_sbh = K->stride[2]; args.k_srow = K->stride[1]; args.k_sshard = K->stride[0];
+  args.v_sbh = V->stride[2]; args.v_srow = V->stride[1]; args.v_sshard = V->stride[0];
+  args.o_sbh = O->stride[2]; args.o_srow = O->stride[1]; args.o_sshard = O->stride[0];
+  args.LSE = static_cast<float *>(LSE->ptr); args.lse_sbh = lse_sbh;
+  args.BH = (int)Hl; args.BHkv = (int)Hl; args.n = (int)n; args.d = (int)d;
+  args.n_loc = (int)n_loc;
+  args.cu_seqlens = nullptr; args.nbatch = 0; args.max_seqlen = 0;
+  args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
+  DevInfo *di = nullptr;
+  if ((rc = device_ready(&di))) return rc;
+  cudaError_t e = launch_attn_fwd_pv16(args, workspace, wait_cfg(di),
+                                       static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return CHAIN_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
+}
+
 // Packed variable-length tensor [total][H][d] bf16: d contiguous, row and
 // head strides in 16-byte multiples, 16-byte aligned.
 static int packed_view(const chain_tensor_t *t, int64_t total, int64_t H, int64_t d) {

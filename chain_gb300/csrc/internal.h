@@ -43,7 +43,8 @@ cudaError_t launch_attn_fwd_fp8(const AttnFwdArgs &a, void *v16, const WaitCfg &
                                cudaStream_t st);
 // bf16 Q, K, V with P V as one f16 product (V re-encoded in f16 with a
 // power-of-two scale per K/V head); ws = attn_fwd_pv16_workspace bytes,
-// 16-byte aligned.  Dense layouts, d = 64 or 128.
+// 16-byte aligned.  Head-major or sequence-shard layouts (n_loc < n), d = 64
+// or 128.
 size_t attn_fwd_pv16_workspace(int BHkv, int n, int d);
 cudaError_t launch_attn_fwd_pv16(const AttnFwdArgs &a, void *ws, const WaitCfg &wc,
                                  cudaStream_t st);

@@ -227,6 +227,24 @@ int chain_fwd_sp(const chain_tensor_t *Q, const chain_tensor_t *K,
                  void *stream);
 
 /*
+ * chain_fwd_sp_f16pv -- chain_fwd_sp with P V taken as one f16 product, as
+ * chain_fwd_f16pv does: Q, K read from and O written to the Ulysses
+ * sequence shards [p][n_loc][H][d] bf16 (same rules as chain_fwd_sp); the
+ * f16 copy of the group's V heads, head-major, is written by a pre-pass that
+ * reads the shards, so V's relayout is part of its re-encoding.
+ *   workspace  at least chain_fwd_sp_f16pv_workspace_size(V, p) bytes,
+ *              16-byte aligned.
+ * Same results, bit for bit, as sp_relayout of Q, K and V, then
+ * chain_fwd_f16pv, then sp_relayout_inverse of O.  Errors as chain_fwd_sp,
+ * plus CHAIN_ERR_ARG for a missing or short workspace.
+ */
+size_t chain_fwd_sp_f16pv_workspace_size(const chain_tensor_t *V, int p);
+int chain_fwd_sp_f16pv(const chain_tensor_t *Q, const chain_tensor_t *K,
+                       const chain_tensor_t *V, int p, int head_group, int mask,
+                       float scale, chain_tensor_t *O, chain_tensor_t *LSE,
+                       void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * chain_fwd_varlen -- softmax attention over a batch of sequences of
  * different lengths packed end to end (the long-sequence regime of "Ulysses
  * Sequence Parallelism", "Contexte Technique", batches sequences of uneven

@@ -106,3 +106,66 @@ def test_sp_full_size_matches_unfused(cg):
     ro, rl = _unfused(cg, q, k, v, p, 0, True, d ** -0.5, o_init)
     assert torch.equal(o.view(torch.int16), ro.view(torch.int16))
     assert torch.equal(lse.view(torch.int32), rl.view(torch.int32))
+
+
+# ------------------------------------------- f16 P V form (chain_fwd_sp_f16pv)
+def _unfused_f16pv(cg, q, k, v, p, g, causal, scale, o_init):
+    """sp_relayout of Q, K, V, chain_fwd_f16pv, inverse relayout of O."""
+    qh, kh, vh = (cg.relayout(x, p, g) for x in (q, k, v))
+    oh, lse = cg.attention_fwd_f16pv(qh, kh, vh, causal, scale)
+    o = o_init.clone()
+    cg.sp_relayout_inverse(oh, p, g, o)
+    return o, lse
+
+
+@pytest.mark.parametrize("p,n_loc,H,d,g,causal", [
+    (4, 256, 8, 128, 0, True), (4, 256, 8, 128, 3, False), (2, 384, 4, 64, 1, True),
+    (1, 512, 2, 128, 0, True), (4, 128, 4, 128, 2, True)])
+def test_sp_f16pv_matches_unfused_bit_exact(cg, p, n_loc, H, d, g, causal):
+    q, k, v = (cs.normal((p, n_loc, H, d), seed=8500 + i).cuda() for i in range(3))
+    scale = 1.0 / math.sqrt(d)
+    o_init = cs.iota16((p, n_loc, H, d)).view(torch.bfloat16).cuda()
+    o, lse = cg.attention_fwd_sp_f16pv(q, k, v, p, g, causal, scale, o=o_init.clone())
+    assert cg.chain_check()[0] == 0
+    ro, rl = _unfused_f16pv(cg, q, k, v, p, g, causal, scale, o_init)
+    assert np.array_equal(_bits(o), _bits(ro)), "O differs from the unfused path"
+    assert np.array_equal(_bits(lse), _bits(rl)), "LSE differs from the unfused path"
+
+
+def test_sp_f16pv_vs_oracle(cg, orc):
+    p, n_loc, H, d, g = 4, 128, 8, 128, 1
+    q, k, v = (cs.normal((p, n_loc, H, d), seed=8600 + i) for i in range(3))
+    scale = d ** -0.5
+    o, lse = cg.attention_fwd_sp_f16pv(q.cuda(), k.cuda(), v.cuda(), p, g, True, scale)
+    assert cg.chain_check()[0] == 0
+    heads = []
+    for x in (q, k, v):
+        raw, shape = orc.relayout(x, p, g)
+        heads.append(torch.from_numpy(raw).view(torch.bfloat16).reshape(shape))
+    ro, rl = orc.softmax_fwd(heads[0], heads[1], heads[2], scale, True)
+    raw, shape = orc.relayout(o.cpu(), p, g)
+    oh = torch.from_numpy(raw).view(torch.bfloat16).reshape(shape)
+    assert_fwd_close(oh, ro, "sharded f16 P V O vs oracle")
+    assert_lse_close(lse, rl, "sharded f16 P V LSE vs oracle")
+
+
+def test_sp_f16pv_rejects_short_workspace(cg):
+    q = torch.zeros(4, 128, 8, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(cg.ChainError) as e:
+        cg.attention_fwd_sp_f16pv(q, q, q, 4, 0, True,
+                                  workspace=torch.empty(64, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == cg.ERR_ARG
+
+
+def test_sp_f16pv_full_size_matches_unfused(cg):
+    dm = cs.WORKLOADS["ulysses_128k"].dims
+    p, n_loc, H, d = dm["p"], dm["n_loc"], dm["H"], dm["d"]
+    gen = torch.Generator(device="cuda").manual_seed(85)
+    q, k, v = (torch.randn(p, n_loc, H, d, device="cuda", generator=gen).to(torch.bfloat16)
+               for _ in range(3))
+    o_init = torch.zeros_like(q)
+    o, lse = cg.attention_fwd_sp_f16pv(q, k, v, p, 0, True, o=o_init.clone())
+    assert cg.chain_check()[0] == 0
+    ro, rl = _unfused_f16pv(cg, q, k, v, p, 0, True, d ** -0.5, o_init)
+    assert torch.equal(o.view(torch.int16), ro.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), rl.view(torch.int32))
