@@ -2,16 +2,18 @@
 
 One step = one pass of every row of the hot path over its full-size
 synthetic workload (seeded, inputs resident in HBM for the kernel-only
-number):
-  * sp_relayout of the Q, K and V sequence shards 4x[32768][32][128] bf16
-    to head-major [8][131072][128] (head group 0),
-  * causal attention forward on those 8 heads at n = 131072, d = 128,
-  * causal attention forward 32 x 32768 x 128 (both through chain_fwd_f16pv:
-    P V as one f16 product, V re-encoded by a two-launch pre-pass that is
-    timed with them; chain_fwd's compensated form is timed beside the step),
+number), in this order (the rows are independent; those with small inputs go
+first so that, end to end, compute starts before all inputs have arrived):
+  * causal attention forward 32 x 32768 x 128 (chain_fwd_f16pv: P V as one
+    f16 product, V re-encoded by a two-launch pre-pass that is timed with it;
+    chain_fwd's compensated form is timed beside the step),
   * GeLU MLP chain 4096x1024 . 1024x4096 . 4096x1024,
   * causal attention backward with recompute 16 x 65536 x 128,
-  * the small fp32 attention 1 x 256 x 64.
+  * the small fp32 attention 1 x 256 x 64,
+  * sp_relayout of the Q, K and V sequence shards 4x[32768][32][128] bf16
+    to head-major [8][131072][128] (head group 0),
+  * causal attention forward on those 8 heads at n = 131072, d = 128
+    (chain_fwd_f16pv).
 value = algorithmic FLOPs of the chain kernels per step / device time per
 step (TFLOP/s).  The relayout contributes bytes, not FLOPs; its GB/s and
 every component's share are reported under "components".
@@ -38,9 +40,9 @@ if ROOT not in sys.path:
 
 METRIC = ("f(AB)C TFLOP/s bf16 (attn fwd/bwd, GeLU MLP) and % of tensor peak; "
           "relayout GB/s")
-WORKLOAD = ("chain hot path: 3x sp_relayout 4x[32768][32][128]->[8][131072][128] + causal "
-            "attn fwd 8x131072x128 + causal attn fwd 32x32768x128 + GeLU MLP "
-            "4096x1024x4096x1024 + causal attn bwd 16x65536x128 + attn fwd fp32 1x256x64")
+WORKLOAD = ("chain hot path: causal attn fwd 32x32768x128 + GeLU MLP 4096x1024x4096x1024 + "
+            "causal attn bwd 16x65536x128 + attn fwd fp32 1x256x64 + 3x sp_relayout "
+            "4x[32768][32][128]->[8][131072][128] + causal attn fwd 8x131072x128")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -244,31 +246,21 @@ class HotPath:
             raise
 
     def _components(self):
+        """The step's components, in launch order.  Each lists the device
+        tensors it reads from the host ("ins") and the results it returns
+        ("outs") for the end-to-end measurement.  The components are
+        independent, so those with small inputs go first: end to end, the
+        first step starts after 0.8 GB of uploads instead of all 5.4 GB."""
         cg = self.cg
         u, c3, m, b, t1 = self.u, self.c3, self.m, self.b, self.t1
         Hl, N = u["H"] // u["p"], u["p"] * u["n_loc"]
         comps = []
-        for t in range(3):
-            comps.append(dict(name=f"sp_relayout[{'QKV'[t]}]", flops=0.0,
-                              bytes=2.0 * Hl * N * u["d"] * 2, launches=1,
-                              kernels=[("relayout_kernel", 0.0, 2.0 * Hl * N * u["d"] * 2)],
-                              fn=(lambda t=t: cg.sp_relayout(self.shards[t], u["p"], u["g"], self.hm[t]))))
-        # the causal forwards: chain_fwd_f16pv (P V as one f16 product); its
-        # V pre-pass (two HBM-bound launches: 2 + 2 bytes read, 2 written per
-        # element) is timed with it
-        pre = "v_absmax_kernel+v_to_f16_kernel"
-        comps.append(dict(name="attn_fwd_causal_8x131072x128", flops=attn_fwd_flops(Hl, N, u["d"], True),
-                          bytes=0.0, launches=3,
-                          kernels=[(pre, 0.0, 6.0 * Hl * N * u["d"]),
-                                   ("attn_fwd_pv16_kernel", attn_fwd_flops(Hl, N, u["d"], True), 0.0)],
-                          fn=lambda: cg.chain_fwd_f16pv(self.hm[0], self.hm[1], self.hm[2],
-                                                        cg.MASK_CAUSAL, u["d"] ** -0.5, self.o4,
-                                                        self.l4, self.ws4)))
         comps.append(dict(name="attn_fwd_causal_32x32768x128",
                           flops=attn_fwd_flops(c3["BH"], c3["n"], c3["d"], True), bytes=0.0, launches=3,
-                          kernels=[(pre, 0.0, 6.0 * c3["BH"] * c3["n"] * c3["d"]),
+                          kernels=[("v_absmax_kernel+v_to_f16_kernel", 0.0, 6.0 * c3["BH"] * c3["n"] * c3["d"]),
                                    ("attn_fwd_pv16_kernel",
                                     attn_fwd_flops(c3["BH"], c3["n"], c3["d"], True), 0.0)],
+                          ins=[self.q3, self.k3, self.v3], outs=[self.o3, self.l3],
                           fn=lambda: cg.chain_fwd_f16pv(self.q3, self.k3, self.v3, cg.MASK_CAUSAL,
                                                         c3["d"] ** -0.5, self.o3, self.l3,
                                                         self.ws3)))
@@ -277,6 +269,7 @@ class HotPath:
                               flops=mlp_flops(m["M"], m["K"], m["N"], m["P"]), bytes=0.0, launches=1,
                               kernels=[("mlp_cluster_kernel", mlp_flops(m["M"], m["K"], m["N"], m["P"]),
                                         0.0)],
+                              ins=[self.x, self.w1, self.w2], outs=[self.o2],
                               fn=lambda: cg.chain_fwd(self.x, self.w1, self.w2, cg.F_GELU_TANH, 0, 1.0,
                                                       self.o2, None)))
         fb = attn_bwd_flops(b["BH"], b["n"], b["d"], True)
@@ -284,6 +277,8 @@ class HotPath:
         # (its recomputed S and dP are not counted)
         comps.append(dict(name="attn_bwd_causal_16x65536x128", flops=fb, bytes=0.0, launches=3,
                           kernels=[("bwd_dkdv_kernel", 0.8 * fb, 0.0), ("bwd_dq_kernel", 0.2 * fb, 0.0)],
+                          ins=[self.q5, self.k5, self.v5, self.do5, self.o5, self.l5],
+                          outs=[self.dq5, self.dk5, self.dv5],
                           fn=lambda: cg.chain_bwd(self.do5, self.q5, self.k5, self.v5, self.o5, self.l5,
                                                   cg.F_SOFTMAX, cg.MASK_CAUSAL, b["d"] ** -0.5,
                                                   self.dq5, self.dk5, self.dv5, self.ws)))
@@ -292,9 +287,27 @@ class HotPath:
                               flops=attn_fwd_flops(1, t1["n"], t1["d"], False), bytes=0.0, launches=1,
                               kernels=[("attn_fwd_f32_kernel", attn_fwd_flops(1, t1["n"], t1["d"], False),
                                         0.0)],
+                              ins=[self.q1, self.k1, self.v1], outs=[self.o1, self.l1],
                               fn=lambda: cg.chain_fwd(self.q1, self.k1, self.v1, cg.F_SOFTMAX,
                                                       cg.MASK_NONE, t1["d"] ** -0.5, self.o1,
                                                       self.l1)))
+        for t in range(3):
+            comps.append(dict(name=f"sp_relayout[{'QKV'[t]}]", flops=0.0,
+                              bytes=2.0 * Hl * N * u["d"] * 2, launches=1,
+                              kernels=[("relayout_kernel", 0.0, 2.0 * Hl * N * u["d"] * 2)],
+                              ins=[self.shards[t]], outs=[],
+                              fn=(lambda t=t: cg.sp_relayout(self.shards[t], u["p"], u["g"], self.hm[t]))))
+        # the causal forward on the relayouted heads: chain_fwd_f16pv (P V as
+        # one f16 product); its V pre-pass (two HBM-bound launches: 2 + 2
+        # bytes read, 2 written per element) is timed with it
+        comps.append(dict(name="attn_fwd_causal_8x131072x128", flops=attn_fwd_flops(Hl, N, u["d"], True),
+                          bytes=0.0, launches=3,
+                          kernels=[("v_absmax_kernel+v_to_f16_kernel", 0.0, 6.0 * Hl * N * u["d"]),
+                                   ("attn_fwd_pv16_kernel", attn_fwd_flops(Hl, N, u["d"], True), 0.0)],
+                          ins=[], outs=[self.o4, self.l4],
+                          fn=lambda: cg.chain_fwd_f16pv(self.hm[0], self.hm[1], self.hm[2],
+                                                        cg.MASK_CAUSAL, u["d"] ** -0.5, self.o4,
+                                                        self.l4, self.ws4)))
         return comps
 
     def step(self, events=None):
@@ -309,20 +322,18 @@ class HotPath:
 
     # host <-> device for the end-to-end number
     def host_io(self, make_host=True):
-        """Device input/output tensors of a step and, if make_host, pinned host
-        copies of the inputs and pinned host buffers for the outputs."""
+        """Per component: its device input and output tensors and, if
+        make_host, pinned host copies of the inputs and pinned host buffers
+        for the outputs."""
         torch = self.torch
-        ins = self.shards + [self.q3, self.k3, self.v3, self.x, self.w1, self.w2, self.q5, self.k5,
-                             self.v5, self.do5, self.o5, self.l5, self.q1, self.k1, self.v1]
-        outs = [self.o4, self.l4, self.o3, self.l3, self.o2, self.dq5, self.dk5, self.dv5, self.o1,
-                self.l1]
-        ins = [t for t in ins if t.numel() > 0]
-        outs = [t for t in outs if t.numel() > 0]
-        if not make_host:
-            return ins, None, outs, None
-        h_in = [t.cpu().pin_memory() for t in ins]
-        h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
-        return ins, h_in, outs, h_out
+        res = []
+        for c in self.comp:
+            ins = [t for t in c["ins"] if t.numel() > 0]
+            outs = [t for t in c["outs"] if t.numel() > 0]
+            h_in = [t.cpu().pin_memory() for t in ins] if make_host else None
+            h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs] if make_host else None
+            res.append((ins, h_in, outs, h_out))
+        return res
 
     @property
     def flops(self):
@@ -766,46 +777,52 @@ def main():
     # ---- end to end through the C ABI with host buffers.  Every step copies
     # its inputs from pinned host memory and its results back.  Two sets of
     # device buffers let step k+1's uploads (own stream) run under step k's
-    # kernels, and step k's downloads (own stream) under step k+1's; events
-    # order each copy after the work whose buffers it touches.
+    # kernels, and step k's downloads (own stream) under step k+1's.  Each
+    # component waits only for its own inputs, and its results leave as soon
+    # as it has finished; events order each copy after the work whose
+    # buffers it touches.
     e2e = None
     if not args.no_e2e:
         hps = [hp, HotPath(dev, only=args.only)]
-        ins0, h_in, outs0, h_out = hp.host_io()
-        io = [(ins0, outs0)]
-        ins1, _, outs1, _ = hps[1].host_io(make_host=False)
-        io.append((ins1, outs1))
-        h2d = sum(t.numel() * t.element_size() for t in h_in)
-        d2h = sum(t.numel() * t.element_size() for t in h_out)
+        io0 = hp.host_io()
+        io1 = hps[1].host_io(make_host=False)
+        io = [io0, io1]
+        h2d = sum(t.numel() * t.element_size() for _, h_in, _, _ in io0 for t in h_in)
+        d2h = sum(t.numel() * t.element_size() for _, _, _, h_out in io0 for t in h_out)
         s_up, s_down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         comp = torch.cuda.Stream(device=dev)
         ev = lambda: torch.cuda.Event(enable_timing=False)
+        ncomp = len(hp.comp)
 
         def run(nsteps, t0=None, t1=None):
-            up = [ev(), ev()]
-            done = [ev(), ev()]
-            down = [ev(), ev()]
+            done = [ev(), ev()]   # step finished with its buffer set
+            down = [ev(), ev()]   # its results are on the host
             if t0 is not None:
                 t0.record(s_up)
             for k in range(nsteps):
                 X = k % 2
-                ins, outs = io[X]
+                up_c = [ev() for _ in range(ncomp)]
+                done_c = [ev() for _ in range(ncomp)]
                 with torch.cuda.stream(s_up):
                     if k >= 2:
                         s_up.wait_event(done[X])  # step k-2 no longer reads these inputs
-                    for d_, h_ in zip(ins, h_in):
-                        d_.copy_(h_, non_blocking=True)
-                    up[X].record(s_up)
-                comp.wait_event(up[X])
+                    for c in range(ncomp):
+                        for d_, h_ in zip(io[X][c][0], io0[c][1]):
+                            d_.copy_(h_, non_blocking=True)
+                        up_c[c].record(s_up)
                 if k >= 2:
                     comp.wait_event(down[X])  # step k-2's results are on the host
                 with torch.cuda.stream(comp):
-                    hps[X].step()
+                    for c in range(ncomp):
+                        comp.wait_event(up_c[c])
+                        hps[X].comp[c]["fn"]()
+                        done_c[c].record(comp)
                     done[X].record(comp)
                 with torch.cuda.stream(s_down):
-                    s_down.wait_event(done[X])
-                    for h_, d_ in zip(h_out, outs):
-                        h_.copy_(d_, non_blocking=True)
+                    for c in range(ncomp):
+                        s_down.wait_event(done_c[c])
+                        for h_, d_ in zip(io0[c][3], io[X][c][2]):
+                            h_.copy_(d_, non_blocking=True)
                     down[X].record(s_down)
             if t1 is not None:
                 s_down.wait_stream(comp)
@@ -822,7 +839,9 @@ def main():
         ms_e2e = max_over_ranks(e0.elapsed_time(e1), dist) / args.steps
         e2e = {"value": round(flops_all / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3),
-               "overlap": "uploads and downloads on their own streams, double-buffered device sets"}
+               "overlap": "uploads and downloads on their own streams, double-buffered device sets; "
+                          "each component waits for its own inputs only and returns its results "
+                          "as soon as it has finished"}
         rc, site = cg.chain_check()
         if rc != 0:
             raise RuntimeError(f"device status {rc} site {site:#x} in e2e region")
