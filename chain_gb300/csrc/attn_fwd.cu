@@ -9,7 +9,8 @@
 // One CTA per (head, 256-row query block) = two 128-row query tiles "a" and
 // "b" that share every K/V tile; CTAs run head by head (K/V reuse in L2),
 // heaviest causal blocks first within a head.
-// Warp roles (320 threads; 384 for 8-bit inputs, warps 10 and 11 idle):
+// Warp roles (320 threads; 384 for the f16 P V kernels, warps 10 and 11
+// idle):
 //   warps 0-3  softmax of tile a, warps 4-7 softmax of tile b: thread t of
 //              a warpgroup owns query row t of its tile.  It reads its row
 //              of S from tensor memory, runs the online softmax in fp32
@@ -31,7 +32,10 @@
 // Tensor memory: S_a/P_a [0,128), S_b/P_b [128,256), O_a [256,384),
 // O_b [384,512).
 //
-// 8-bit inputs (attn_fwd_fp8_kernel): Q and K in e4m3, S = Q K^T by the
+// f16 P V (attn_fwd_pv16_kernel, attn_fwd_sp_pv16_kernel: bf16 Q, K, V;
+// attn_fwd_fp8_kernel: e4m3 Q, K, V): P enters one f16 P V product and V an
+// f16 copy made by a pre-pass (bf16: per K/V head scaled by a power of two,
+// undone in the epilogue).  8-bit inputs: Q and K in e4m3, S = Q K^T by the
 // kind::f8f6f4 tensor-core product (K = 32 per instruction, one 128-byte
 // swizzled row per d = 128 row).  P is written back as one f16 per key
 // (keys [32g, 32g+32) in columns [16g, 16g+16)): f16 keeps 11 significant
@@ -46,17 +50,17 @@ namespace {
 constexpr int BM = 128;  // rows per query tile (two tiles per CTA)
 constexpr int BN = 128;  // keys per K/V tile
 constexpr int STAGES = 2;
-// Threads a CTA: 320 for bf16 (8 softmax warps, producer, MMA; 168
+// Threads a CTA: 320 for the compensated bf16 kernel (8 softmax warps, producer, MMA; 168
 // registers, three warps per scheduler filling its quarter of the register
-// file).  For 8-bit inputs 384 at 168 registers (384 x 168 = 64,512 of the
+// file).  For the f16 P V kernels 384 at 168 registers (384 x 168 = 64,512 of the
 // SM's 65,536): the producer/MMA warpgroup (with two idle warps) gives back
 // down to 136 and the softmax warpgroups take 184, so that a row of S stays
 // in registers next to the packed arithmetic's register pairs:
 // 256 x 184 + 128 x 136 = 64,512, and 184 + 184 + 136 <= 512 per scheduler.
-// (The same split measured 2-3% slower for bf16 at n = 131072.)
+// (The same split measured 2-3% slower for the compensated kernel at n = 131072.)
 template <bool PV16>
 constexpr int fwd_threads() { return PV16 ? 384 : 320; }
-constexpr uint32_t REGS_SOFTMAX = 184, REGS_CONTROL = 136;  // 8-bit inputs
+constexpr uint32_t REGS_SOFTMAX = 184, REGS_CONTROL = 136;  // f16 P V kernels
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 
 template <int D, bool QK8>
@@ -223,7 +227,7 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // The three roles; 8-bit inputs reallocate registers per warpgroup
+  // The three roles; the f16 P V kernels reallocate registers per warpgroup
   // before running theirs.
   auto role_producer = [&]() {
     // ------------------------------------------------------ TMA producer
@@ -316,7 +320,7 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
             umma_f16_ss(tmem + t * BN, sdesc_at(a, off), sdesc_at(b, off), idS, kk > 0 ? 1u : 0u);
         }
       };
-      // O_t += P_hi V_j + P_lo V_j (8-bit inputs: O_t += P V_j, one f16 P
+      // O_t += P_hi V_j + P_lo V_j (f16 P V: O_t += P V_j, one f16 P
       // per key), P read from tensor memory
       auto issue_pv = [&](int t, int j) {
         const SDesc b = (j & 1) ? dV1 : dV0;
