@@ -16,7 +16,9 @@ def cg():
 
 
 @pytest.mark.parametrize("p,n_loc,H,d,g", [
-    (4, 37, 8, 128, 0), (4, 37, 8, 128, 3), (2, 5, 6, 64, 1), (4, 1, 4, 8, 2), (1, 19, 3, 128, 0)])
+    (4, 37, 8, 128, 0), (4, 37, 8, 128, 3), (2, 5, 6, 64, 1), (4, 1, 4, 8, 2), (1, 19, 3, 128, 0),
+    # more positions than one grid pass, 2 KB rows, a group of 512 heads
+    (4, 300, 8, 128, 1), (2, 16, 4, 1024, 1), (1, 7, 512, 8, 0)])
 def test_relayout_iota_bit_exact(cg, orc, p, n_loc, H, d, g):
     x = cs.iota16((p, n_loc, H, d))
     out = cg.relayout(x.cuda(), p, g)
