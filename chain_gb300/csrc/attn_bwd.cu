@@ -448,12 +448,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const float4 lv = wl4[c4];
           const float ls[4] = {lv.x, lv.y, lv.z, lv.w};
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int qq = 4 * c4 + u;
-            float pr = ex2(fmaf(__uint_as_float(sv[qq]), p.scale_log2, -ls[u]));
-            if (!kv_ok || (diag && 64 * w + qq < r)) pr = 0.0f;  // a select, no branch
-            pf[qq] = pr;
-          }
+          for (int u = 0; u < 4; ++u)
+            pf[4 * c4 + u] = ex2(fmaf(__uint_as_float(sv[4 * c4 + u]), p.scale_log2, -ls[u]));
+        }
+        // key beyond n, or (diagonal tile) query before the key: one branch
+        // around the whole pass, none in the loop above
+        if (!kv_ok || diag) {
+#pragma unroll
+          for (int qq = 0; qq < 64; ++qq)
+            if (!kv_ok || 64 * w + qq < r) pf[qq] = 0.0f;
         }
       }
       {
