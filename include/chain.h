@@ -130,7 +130,8 @@ size_t chain_bwd_workspace_size_f(const chain_tensor_t *A, const chain_tensor_t 
 /*
  * chain_bwd -- gradients of the softmax chain (attention backward).
  *   Inputs: dO, Q (A), K (B), V (C), O [BH][n][d] bf16 and LSE [BH][n] f32
- *   as produced by chain_fwd with the same f, mask and scale.  Only
+ *   as produced by chain_fwd (or chain_fwd_f16pv) with the same f, mask and
+ *   scale.  Only
  *   f = CHAIN_F_SOFTMAX with bf16 and d in {64, 128} is supported.
  *   Outputs: dQ (dA), dK (dB), dV (dC) [BH][n][d] bf16.  With grouped-query
  *   attention K, V, dK, dV are [BHkv][n][d] and dK, dV sum over the query
