@@ -724,6 +724,7 @@ int chain_fwd_f16pv(const chain_tensor_t *Q, const chain_tensor_t *K, const chai
   if (!workspace || !aligned16(workspace) ||
       ws_bytes < attn_fwd_pv16_workspace((int)v.outer, (int)v.rows, (int)v.cols))
     return CHAIN_ERR_ARG;
+  if (v.outer > 65535) return CHAIN_ERR_UNSUPPORTED;  // the V pre-pass grid's y extent
   AttnFwdArgs args;
   args.Q = q.ptr; args.K = k.ptr; args.V = v.ptr;
   args.q_sbh = q.s_outer; args.q_srow = q.s_row;

@@ -310,7 +310,8 @@ int chain_bwd_varlen(const chain_tensor_t *dO, const chain_tensor_t *Q,
  * of it.  The epilogue undoes the scale.  Error: one bf16 rounding of O plus
  * P's f16 rounding (~2^-12 relative, random over the keys).  Returns
  * CHAIN_ERR_DTYPE unless bf16, CHAIN_ERR_ARG for a shape, stride, alignment
- * or workspace violation.  Asynchronous on `stream`.
+ * or workspace violation, CHAIN_ERR_UNSUPPORTED for more than 65,535 K/V
+ * heads.  Asynchronous on `stream`.
  */
 size_t chain_fwd_f16pv_workspace_size(const chain_tensor_t *Q, const chain_tensor_t *V);
 int chain_fwd_f16pv(const chain_tensor_t *Q, const chain_tensor_t *K,
