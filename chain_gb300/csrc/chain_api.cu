@@ -581,6 +581,7 @@ int chain_fwd_sp_f16pv(const chain_tensor_t *Q, const chain_tensor_t *K, const c
   if (!workspace || !aligned16(workspace) ||
       ws_bytes < attn_fwd_pv16_workspace((int)Hl, (int)n, (int)d))
     return CHAIN_ERR_ARG;
+  if (Hl > 65535) return CHAIN_ERR_UNSUPPORTED;  // the V pre-pass grid's y extent
   const int64_t h0 = (int64_t)head_group * Hl;
   AttnFwdArgs args;
   args.Q = static_cast<const __nv_bfloat16 *>(Q->ptr) + h0 * Q->stride[2];
