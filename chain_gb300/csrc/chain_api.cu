@@ -218,7 +218,7 @@ const char *chain_status_string(int status) {
     case CHAIN_ERR_DEVICE: return "current device is not compute capability 10.3";
     case CHAIN_ERR_CUDA: return "CUDA call failed (see chain_last_cuda_error)";
     case CHAIN_ERR_TIMEOUT: return "a bounded device-side wait expired";
-    case CHAIN_ERR_UNSUPPORTED: return "request not implemented by this build";
+    case CHAIN_ERR_UNSUPPORTED: return "valid request this library does not implement";
     case CHAIN_ERR_SCRATCH_LIMIT:
       return "problem needs more scratch than the fixed array of chain_bwd_noalloc";
     default: return "unknown status";

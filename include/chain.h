@@ -55,7 +55,7 @@ typedef enum {
   CHAIN_ERR_DEVICE = -3,  /* current device is not compute capability 10.3 */
   CHAIN_ERR_CUDA = -4,    /* a CUDA runtime/driver call failed */
   CHAIN_ERR_TIMEOUT = -5, /* a bounded device-side wait expired */
-  CHAIN_ERR_UNSUPPORTED = -6, /* valid request this build does not implement */
+  CHAIN_ERR_UNSUPPORTED = -6, /* valid request this library does not implement */
   CHAIN_ERR_SCRATCH_LIMIT = -7 /* problem needs more than CHAIN_NOALLOC_SCRATCH_BYTES */
 } chain_status_t;
 
