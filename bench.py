@@ -649,6 +649,118 @@ def measure_fwd_compensated(hp, reps=5):
     return out
 
 
+def _median_ms(torch, fn, reps, warm=2):
+    """Median device time of fn() over reps calls on the current stream."""
+    for _ in range(warm):
+        fn()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return sorted(ts)[len(ts) // 2]
+
+
+def measure_gqa(hp, reps=5):
+    """Grouped-query attention, 32 query heads over 8 K/V heads at n = 32768,
+    causal: forward (chain_fwd_f16pv) and backward (chain_bwd), each timed
+    as one call.  Measured beside the step, not part of its value."""
+    torch, cg, cs = hp.torch, hp.cg, hp.cs
+    wl = cs.WORKLOADS["gqa_32k"]
+    dm = wl.dims
+    BH, BHkv, n, d = dm["BH"], dm["BHkv"], dm["n"], dm["d"]
+    q, _, _, do = cs.attn_inputs(BH, n, d, seed=wl.seed, device=hp.dev, with_do=True)
+    k = cs.normal((BHkv, n, d), wl.seed + cs.OFF_K, device=hp.dev)
+    v = cs.normal((BHkv, n, d), wl.seed + cs.OFF_V, device=hp.dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(BH, n, dtype=torch.float32, device=hp.dev)
+    wsf = torch.empty(max(cg.chain_fwd_f16pv_workspace_size(q, v), 16), dtype=torch.uint8,
+                      device=hp.dev)
+    wsb = torch.empty(cg.chain_bwd_workspace_size(q, v), dtype=torch.uint8, device=hp.dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    scale = d ** -0.5
+
+    def fwd():
+        cg.chain_fwd_f16pv(q, k, v, cg.MASK_CAUSAL, scale, o, lse, wsf)
+
+    def bwd():
+        cg.chain_bwd(do, q, k, v, o, lse, cg.F_SOFTMAX, cg.MASK_CAUSAL, scale, dq, dk, dv, wsb)
+
+    ms_f = _median_ms(torch, fwd, reps)
+    ms_b = _median_ms(torch, bwd, reps)
+    rc, site = cg.chain_check()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} site {site:#x} in the grouped-query measurement")
+    ff, fb = attn_fwd_flops(BH, n, d, True), attn_bwd_flops(BH, n, d, True)
+    del q, k, v, do, o, lse, wsf, wsb, dq, dk, dv
+    return {"attn_gqa_causal_32q8kv_x32768x128": {
+        "fwd_ms": round(ms_f, 4), "fwd_TFLOPs": round(ff / (ms_f * 1e-3) / 1e12, 1),
+        "bwd_ms": round(ms_b, 4), "bwd_TFLOPs": round(fb / (ms_b * 1e-3) / 1e12, 1),
+        "calls": "chain_fwd_f16pv, chain_bwd",
+        "timing": f"median of {reps} after 2 warm-ups; inputs larger than L2"}}
+
+
+def measure_varlen(hp, reps=5):
+    """Sequences of mixed lengths (seeded, 1024..16384) packed end to end into
+    131072 positions with 16 heads, causal: forward (chain_fwd_varlen_f16pv;
+    the compensated chain_fwd_varlen beside it) and backward
+    (chain_bwd_varlen).  FLOPs are counted per sequence.  Measured beside the
+    step, not part of its value."""
+    torch, cg, cs = hp.torch, hp.cg, hp.cs
+    wl = cs.WORKLOADS["varlen_128k"]
+    dm = wl.dims
+    total, H, d = dm["total"], dm["H"], dm["d"]
+    lens = cs.varlen_lengths(total, dm["min_len"], dm["max_len"], wl.seed)
+    q = cs.normal((total, H, d), wl.seed + cs.OFF_Q, device=hp.dev)
+    k = cs.normal((total, H, d), wl.seed + cs.OFF_K, device=hp.dev)
+    v = cs.normal((total, H, d), wl.seed + cs.OFF_V, device=hp.dev)
+    do = cs.normal((total, H, d), wl.seed + cs.OFF_DO, device=hp.dev)
+    cu_host = [0]
+    for L in lens:
+        cu_host.append(cu_host[-1] + L)
+    cu = torch.tensor(cu_host, dtype=torch.int32, device=hp.dev)
+    B, mx = len(lens), max(lens)
+    o = torch.empty_like(q)
+    lse = torch.empty(H, total, dtype=torch.float32, device=hp.dev)
+    ws = torch.empty(cg.chain_bwd_workspace_size(q, q), dtype=torch.uint8, device=hp.dev)
+    wsf = torch.empty(cg.chain_fwd_varlen_f16pv_workspace_size(v), dtype=torch.uint8,
+                      device=hp.dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    scale = d ** -0.5
+
+    def fwd():
+        cg.chain_fwd_varlen_f16pv(q, k, v, cu, B, mx, cg.MASK_CAUSAL, scale, o, lse, wsf)
+
+    def fwd_compensated():
+        cg.chain_fwd_varlen(q, k, v, cu, B, mx, cg.MASK_CAUSAL, scale, o, lse)
+
+    def bwd():
+        cg.chain_bwd_varlen(do, q, k, v, o, lse, cu, B, mx, cg.MASK_CAUSAL, scale, dq, dk, dv, ws)
+
+    ms_c = _median_ms(torch, fwd_compensated, reps)
+    ms_f = _median_ms(torch, fwd, reps)
+    ms_b = _median_ms(torch, bwd, reps)
+    rc, site = cg.chain_check()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} site {site:#x} in the varlen measurement")
+    ff = sum(attn_fwd_flops(H, L, d, True) for L in lens)
+    fb = sum(attn_bwd_flops(H, L, d, True) for L in lens)
+    del q, k, v, do, o, lse, ws, wsf, dq, dk, dv, cu
+    return {"attn_varlen_causal_131072x16x128": {
+        "fwd_ms": round(ms_f, 4), "fwd_TFLOPs": round(ff / (ms_f * 1e-3) / 1e12, 1),
+        "compensated_fwd_ms": round(ms_c, 4),
+        "compensated_fwd_TFLOPs": round(ff / (ms_c * 1e-3) / 1e12, 1),
+        "bwd_ms": round(ms_b, 4), "bwd_TFLOPs": round(fb / (ms_b * 1e-3) / 1e12, 1),
+        "sequences": B, "min_len": min(lens), "max_len": mx,
+        "calls": "chain_fwd_varlen_f16pv (compensated: chain_fwd_varlen), chain_bwd_varlen",
+        "flops": "per sequence: fwd 2 n^2 d H, bwd 5 n^2 d H (causal)",
+        "timing": f"median of {reps} after 2 warm-ups; inputs larger than L2"}}
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -680,6 +792,10 @@ def main():
         nxt = {}
         if "fp8" in (args.only or ""):
             nxt.update(measure_fp8(hp))
+        if "gqa" in (args.only or ""):
+            nxt.update(measure_gqa(hp))
+        if "varlen" in (args.only or ""):
+            nxt.update(measure_varlen(hp))
         if rank == 0:
             print(json.dumps({"only": args.only, "next_rows": nxt or None}))
         if dist is not None:
@@ -857,6 +973,10 @@ def main():
         nxt.update(measure_fp8(hp))
     if hp.q3.numel() or hp.hm[0].numel():
         nxt.update(measure_fwd_compensated(hp))
+    if args.only is None or "gqa" in args.only:
+        nxt.update(measure_gqa(hp))
+    if args.only is None or "varlen" in args.only:
+        nxt.update(measure_varlen(hp))
     nxt = nxt or None
 
     cpu = None

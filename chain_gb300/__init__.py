@@ -81,6 +81,10 @@ def _load():
             lib.chain_fwd_f16pv_workspace_size.argtypes = [P, P]
             lib.chain_fwd_sp_f16pv.argtypes = [P, P, P, ci, ci, ci, fl, P, P, vp, ctypes.c_size_t,
                                                vp]
+            lib.chain_fwd_varlen_f16pv.argtypes = [P, P, P, vp, ci, ci, ci, fl, P, P, vp,
+                                                   ctypes.c_size_t, vp]
+            lib.chain_fwd_varlen_f16pv_workspace_size.argtypes = [P]
+            lib.chain_fwd_varlen_f16pv_workspace_size.restype = ctypes.c_size_t
             lib.chain_fwd_sp_f16pv_workspace_size.argtypes = [P, ci]
             lib.chain_fwd_sp_f16pv_workspace_size.restype = ctypes.c_size_t
             lib.chain_fwd_f16pv_workspace_size.restype = ctypes.c_size_t
@@ -225,6 +229,23 @@ def chain_fwd_varlen(Q, K, V, cu_seqlens, batch, max_seqlen, mask, scale, O, LSE
                                  ctypes.c_void_p(cu_seqlens.data_ptr()), int(batch), int(max_seqlen),
                                  int(mask), float(scale), _ref(desc(O)), _ref(desc(LSE)),
                                  _stream(stream)), "chain_fwd_varlen")
+
+
+def chain_fwd_varlen_f16pv(Q, K, V, cu_seqlens, batch, max_seqlen, mask, scale, O, LSE, workspace,
+                           stream=None):
+    """chain_fwd_varlen with P V as one f16 product; see include/chain.h."""
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+        raise ValueError("cu_seqlens must be a CUDA int32 tensor")
+    _ok(_load().chain_fwd_varlen_f16pv(_ref(desc(Q)), _ref(desc(K)), _ref(desc(V)),
+                                       ctypes.c_void_p(cu_seqlens.data_ptr()), int(batch),
+                                       int(max_seqlen), int(mask), float(scale), _ref(desc(O)),
+                                       _ref(desc(LSE)), ctypes.c_void_p(workspace.data_ptr()),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream(stream)), "chain_fwd_varlen_f16pv")
+
+
+def chain_fwd_varlen_f16pv_workspace_size(V) -> int:
+    return int(_load().chain_fwd_varlen_f16pv_workspace_size(_ref(desc(V))))
 
 
 def chain_bwd_varlen(dO, Q, K, V, O, LSE, cu_seqlens, batch, max_seqlen, mask, scale, dQ, dK, dV,
@@ -386,6 +407,20 @@ def attention_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool,
     lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=q.device)
     chain_fwd_varlen(q, k, v, cu_seqlens, cu_seqlens.numel() - 1, max_seqlen,
                      MASK_CAUSAL if causal else MASK_NONE, scale, o, lse, stream)
+    return o, lse
+
+
+def attention_fwd_varlen_f16pv(q, k, v, cu_seqlens, max_seqlen: int, causal: bool,
+                               scale: float | None = None, workspace=None, stream=None):
+    """attention_fwd_varlen with P V as one f16 product: returns (O, LSE)."""
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(max(chain_fwd_varlen_f16pv_workspace_size(v), 16),
+                                dtype=torch.uint8, device=q.device)
+    chain_fwd_varlen_f16pv(q, k, v, cu_seqlens, cu_seqlens.numel() - 1, max_seqlen,
+                           MASK_CAUSAL if causal else MASK_NONE, scale, o, lse, workspace, stream)
     return o, lse
 
 

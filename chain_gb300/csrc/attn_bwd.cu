@@ -218,12 +218,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     bkv = blockIdx.x / p.nb;
     jb = blockIdx.x % p.nb;
   } else {
+    // Within a K/V head, key blocks run in decreasing work over all of the
+    // batch's sequences: causal key block jb meets nb - jb query tiles, so
+    // blocks go by that count, largest first (without a mask, the longest
+    // sequences go first).
     const int per_head = p.nbatch * p.nb;
     bkv = blockIdx.x / per_head;
-    jb = blockIdx.x % p.nb;
-    seq_bounds(p, (blockIdx.x % per_head) / p.nb, row0, n);
+    const int qd = (blockIdx.x % per_head) / p.nbatch;
+    seq_bounds(p, blockIdx.x % p.nbatch, row0, n);
     nb = (n + BM - 1) / BM;
-    if (jb >= nb) return;  // nothing of this sequence for this CTA
+    if (nb > p.nb) {  // longer than the stated maximum: reported, not computed
+      if (qd == 0 && threadIdx.x == 0 && bkv == 0) atomicExch(&p.wc.status->reserved[0], 1);
+      return;
+    }
+    const int jr = p.nb - 1 - qd;
+    jb = p.causal ? nb - 1 - jr : jr;
+    if (jb < 0 || jb >= nb) return;  // nothing of this sequence for this CTA
   }
   const int i_begin = p.causal ? jb : 0;
   const int T = (nb - i_begin) * p.G;
@@ -550,13 +560,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     bh = blockIdx.x / p.nb;
     ib = p.causal ? (p.nb - 1 - (int)(blockIdx.x % p.nb)) : (int)(blockIdx.x % p.nb);
   } else {
+    // Within a head, query tiles run in decreasing position over all of the
+    // batch's sequences: causal tile ib meets ib + 1 key blocks, so the
+    // heaviest go first (without a mask, the longest sequences go first).
     const int per_head = p.nbatch * p.nb;
     bh = blockIdx.x / per_head;
-    const int k = blockIdx.x % p.nb;
-    seq_bounds(p, (blockIdx.x % per_head) / p.nb, row0, n);
+    const int qd = (blockIdx.x % per_head) / p.nbatch;
+    seq_bounds(p, blockIdx.x % p.nbatch, row0, n);
     nb = (n + BM - 1) / BM;
-    if (k >= nb) return;  // nothing of this sequence for this CTA
-    ib = p.causal ? nb - 1 - k : k;
+    if (nb > p.nb) return;  // longer than the stated maximum: reported by the dK, dV kernel
+    ib = p.nb - 1 - qd;
+    if (ib >= nb) return;  // nothing of this sequence for this CTA
   }
   const int NJ = p.causal ? ib + 1 : nb;
 
@@ -832,6 +846,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 template <int D>
 cudaError_t launch_bwd_d(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t st) {
   using L = BwdLayout<D>;
+  const bool varlen = a.cu_seqlens != nullptr;
+  // blocks per head come from the longest sequence of a variable-length batch
+  const int nb_max = ((varlen ? a.max_seqlen : a.n) + BM - 1) / BM;
+  const int64_t nseq = varlen ? a.nbatch : 1;
+  // one CTA per (head, sequence, 128-row block): many short sequences beside
+  // one long one can exceed the grid's x extent; refused before any launch
+  if ((int64_t)nb_max * a.BH * nseq > 0x7fffffff) return cudaErrorNotSupported;
   cudaError_t e;
   {
     const int64_t rows = (int64_t)a.BH * a.n;  // every (head, position)
@@ -855,8 +876,7 @@ cudaError_t launch_bwd_d(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t s
   BwdParams p;
   p.BH = a.BH;
   p.n = a.n;
-  // with a variable-length batch, blocks per head come from the longest sequence
-  p.nb = ((a.cu_seqlens ? a.max_seqlen : a.n) + BM - 1) / BM;
+  p.nb = nb_max;
   p.causal = a.causal;
   p.G = a.BH / a.BHkv;
   p.q_srow = a.q_srow;
@@ -876,15 +896,14 @@ cudaError_t launch_bwd_d(const AttnBwdArgs &a, const WaitCfg &wc, cudaStream_t s
   p.dK = static_cast<__nv_bfloat16 *>(a.dK);
   p.dV = static_cast<__nv_bfloat16 *>(a.dV);
   p.wc = wc;
-  const bool varlen = a.cu_seqlens != nullptr;
   auto ka = varlen ? bwd_dkdv_kernel<D, true> : bwd_dkdv_kernel<D, false>;
   auto kb = varlen ? bwd_dq_kernel<D, true> : bwd_dq_kernel<D, false>;
   if ((e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, L::A_ALLOC)))
     return e;
   if ((e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, L::B_ALLOC)))
     return e;
-  const unsigned nseq = varlen ? (unsigned)a.nbatch : 1u;
-  const unsigned grid_kv = (unsigned)(p.nb * a.BHkv) * nseq, grid_q = (unsigned)(p.nb * a.BH) * nseq;
+  const unsigned grid_kv = (unsigned)((int64_t)p.nb * a.BHkv * nseq);
+  const unsigned grid_q = (unsigned)((int64_t)p.nb * a.BH * nseq);
   timing_mark(st, 0);
   ka<<<grid_kv, NTHREADS, L::A_ALLOC, st>>>(mq, mk, mv, mdo, p);
   timing_mark(st, 1);

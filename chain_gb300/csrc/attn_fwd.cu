@@ -144,7 +144,6 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
   constexpr bool QK8 = MODE == 2;   // e4m3 Q, K
   constexpr bool PV16 = MODE != 0;  // one f16 P V product
   static_assert(!QK8 || D == 128, "8-bit inputs: d = 128 only");
-  static_assert(!PV16 || !VARLEN, "f16 P V: no packed sequences");
   static_assert(!QK8 || !SHARDED, "8-bit inputs: head-major layout only");
   using L = FwdLayout<D, QK8>;
   // Q/K boxes: 128-byte rows of 64 bf16 or 128 e4m3 elements
@@ -177,20 +176,26 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
     qb = p.causal ? (p.nqb2 - 1 - blk % p.nqb2) : (blk % p.nqb2);
   } else {
     // one sequence of a variable-length batch; bounds clamped to the packed
-    // tensor so a bad cu can never address memory outside it
+    // tensor so a bad cu can never address memory outside it.  Within a
+    // head, query-block pairs run in decreasing position over all of the
+    // batch's sequences: a causal pair's work grows with its position, so
+    // the heaviest pairs go first and the lightest fill the tail (without
+    // a mask, the longest sequences go first).
     const int per_head = p.nbatch * p.nqb2;
     bh = blk / per_head;
-    const int b = (blk % per_head) / p.nqb2, k = blk % p.nqb2;
+    const int qd = (blk % per_head) / p.nbatch, b = blk % p.nbatch;
     int lo = __ldg(p.cu + b), hi = __ldg(p.cu + b + 1);
     lo = lo < 0 ? 0 : (lo > p.n ? p.n : lo);
     hi = hi < lo ? lo : (hi > p.n ? p.n : hi);
     row0 = lo;
     n = hi - lo;
     const int nqb2_b = (n + 2 * BM - 1) / (2 * BM);
-    if (nqb2_b > p.nqb2 && k == 0 && threadIdx.x == 0 && bh == 0)
-      atomicExch(&p.wc.status->reserved[0], 1);  // sequence longer than the stated maximum
-    if (k >= nqb2_b) return;  // nothing of this sequence for this CTA
-    qb = p.causal ? nqb2_b - 1 - k : k;
+    if (nqb2_b > p.nqb2) {  // longer than the stated maximum: reported, not computed
+      if (qd == 0 && threadIdx.x == 0 && bh == 0) atomicExch(&p.wc.status->reserved[0], 1);
+      return;
+    }
+    qb = p.nqb2 - 1 - qd;
+    if (qb >= nqb2_b) return;  // nothing of this sequence for this CTA
   }
   const int nkb = (n + BN - 1) / BN;
   const int nkv_a = kv_tiles(p, nkb, qb, 0);
@@ -273,7 +278,7 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
         for (int c = 0; c < D / 64; ++c) {
           uint8_t *dst = smem + L::OFF_V + st * L::V_BYTES + c * (BN * 128);
           if constexpr (PV16)  // the f16 copy of V is head-major in every layout
-            tma_load_3d(dst, &tmV, &v_full[st], c * 64, j * BN, bkv);
+            tma_load_3d(dst, &tmV, &v_full[st], c * 64, row0 + j * BN, bkv);
           else
             load(dst, &tmV, &v_full[st], c * 64, j * BN, bkv);
         }
@@ -617,6 +622,16 @@ __global__ void __launch_bounds__(fwd_threads<true>(), 1)
   attn_fwd_body<D, false, false, 1>(tmQ, tmK, tmV, p);
 }
 
+// The same over sequences packed end to end ([total][H][d], cu_seqlens);
+// V's f16 copy is [Hkv][total][d].
+template <int D>
+__global__ void __launch_bounds__(fwd_threads<true>(), 1)
+    attn_fwd_varlen_pv16_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                const __grid_constant__ CUtensorMap tmK,
+                                const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  attn_fwd_body<D, false, true, 1>(tmQ, tmK, tmV, p);
+}
+
 // The same over Ulysses sequence shards: Q, K read from and O written to
 // [p][n_loc][H][d]; V's f16 copy is head-major (its pre-pass reads the shards).
 template <int D>
@@ -801,7 +816,11 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t s
                       : (a.cu_seqlens ? attn_fwd_kernel<D, false, true> : attn_fwd_kernel<D, false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(p.nqb2 * a.BH * (a.cu_seqlens ? a.nbatch : 1));
+  // one CTA per (head, sequence, query-block pair): many short sequences
+  // beside one long one can exceed the grid's x extent
+  const int64_t grid64 = (int64_t)p.nqb2 * a.BH * (a.cu_seqlens ? a.nbatch : 1);
+  if (grid64 > 0x7fffffff) return cudaErrorNotSupported;
+  const unsigned grid = (unsigned)grid64;
   timing_mark(st, 0);
   kern<<<grid, fwd_threads<false>(), L::ALLOC, st>>>(mq, mk, mv, p);
   timing_mark(st, 1);
@@ -885,6 +904,12 @@ template <int D>
 static cudaError_t launch_pv16_d(const AttnFwdArgs &a, void *ws, const WaitCfg &wc,
                                  cudaStream_t st) {
   using L = FwdLayout<D, false>;
+  // with a variable-length batch, blocks per head come from the longest
+  // sequence; one CTA per (head, sequence, query-block pair), refused before
+  // any launch when that exceeds the grid's x extent
+  const int nqb2 = ((a.cu_seqlens ? a.max_seqlen : a.n) + 2 * BM - 1) / (2 * BM);
+  const int64_t grid64 = (int64_t)nqb2 * a.BH * (a.cu_seqlens ? a.nbatch : 1);
+  if (grid64 > 0x7fffffff) return cudaErrorNotSupported;
   const int nch = (a.n + VCH_ROWS - 1) / VCH_ROWS;
   uint8_t *base = static_cast<uint8_t *>(ws);
   const size_t vb = ((size_t)2 * a.BHkv * a.n * D + 255) & ~(size_t)255;
@@ -929,9 +954,9 @@ static cudaError_t launch_pv16_d(const AttnFwdArgs &a, void *ws, const WaitCfg &
   FwdParams p;
   p.BH = a.BH;
   p.n = a.n;
-  p.cu = nullptr;
-  p.nbatch = 0;
-  p.nqb2 = (a.n + 2 * BM - 1) / (2 * BM);
+  p.cu = a.cu_seqlens;
+  p.nbatch = a.cu_seqlens ? a.nbatch : 0;
+  p.nqb2 = nqb2;
   p.nkb = (a.n + BN - 1) / BN;
   p.causal = a.causal;
   p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -946,18 +971,20 @@ static cudaError_t launch_pv16_d(const AttnFwdArgs &a, void *ws, const WaitCfg &
   p.LSE = a.LSE;
   p.lse_sbh = a.lse_sbh;
   p.wc = wc;
-  auto kern = sharded ? attn_fwd_sp_pv16_kernel<D> : attn_fwd_pv16_kernel<D>;
+  auto kern = sharded ? attn_fwd_sp_pv16_kernel<D>
+                      : (a.cu_seqlens ? attn_fwd_varlen_pv16_kernel<D> : attn_fwd_pv16_kernel<D>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)grid64;
   timing_mark(st, 1);
-  kern<<<(unsigned)(p.nqb2 * a.BH), fwd_threads<true>(), L::ALLOC, st>>>(mq, mk, mv, p);
+  kern<<<grid, fwd_threads<true>(), L::ALLOC, st>>>(mq, mk, mv, p);
   timing_mark(st, 2);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attn_fwd_pv16(const AttnFwdArgs &a, void *ws, const WaitCfg &wc,
                                  cudaStream_t st) {
-  if (a.cu_seqlens) return cudaErrorNotSupported;
+  if (a.cu_seqlens && a.n_loc != a.n) return cudaErrorNotSupported;
   if (a.d == 128) return launch_pv16_d<128>(a, ws, wc, st);
   if (a.d == 64) return launch_pv16_d<64>(a, ws, wc, st);
   return cudaErrorInvalidValue;

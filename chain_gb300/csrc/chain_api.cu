@@ -649,6 +649,57 @@ int chain_fwd_varlen(const chain_tensor_t *Q, const chain_tensor_t *K, const cha
   DevInfo *di = nullptr;
   if ((rc = device_ready(&di))) return rc;
   cudaError_t e = launch_attn_fwd_bf16(args, wait_cfg(di), static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return CHAIN_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
+}
+
+size_t chain_fwd_varlen_f16pv_workspace_size(const chain_tensor_t *V) {
+  if (!V || V->ndim != 3) return 0;
+  const int64_t total = V->shape[0], Hkv = V->shape[1], d = V->shape[2];
+  if (total < 1 || total > (1 << 30) || Hkv < 1 || Hkv > 65535 || (d != 64 && d != 128))
+    return 0;
+  return attn_fwd_pv16_workspace((int)Hkv, (int)total, (int)d);
+}
+
+int chain_fwd_varlen_f16pv(const chain_tensor_t *Q, const chain_tensor_t *K,
+                           const chain_tensor_t *V, const int32_t *cu_seqlens, int batch,
+                           int max_seqlen, int mask, float scale, chain_tensor_t *O,
+                           chain_tensor_t *LSE, void *workspace, size_t ws_bytes, void *stream) {
+  if (!Q || Q->ndim != 3 || !K || K->ndim != 3) return CHAIN_ERR_ARG;
+  if (mask != CHAIN_MASK_NONE && mask != CHAIN_MASK_CAUSAL) return CHAIN_ERR_ARG;
+  const int64_t total = Q->shape[0], H = Q->shape[1], d = Q->shape[2], Hkv = K->shape[1];
+  int rc;
+  if ((rc = packed_view(Q, total, H, d)) || (rc = packed_view(K, total, Hkv, d)) ||
+      (rc = packed_view(V, total, Hkv, d)) || (rc = packed_view(O, total, H, d)))
+    return rc;
+  if (total < 1 || total > (1 << 30) || (d != 64 && d != 128)) return CHAIN_ERR_ARG;
+  if (Hkv < 1 || H % Hkv || H > 65535 * 16) return CHAIN_ERR_ARG;
+  if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return CHAIN_ERR_ARG;
+  if (batch < 1 || batch > (1 << 20) || max_seqlen < 1 || max_seqlen > total) return CHAIN_ERR_ARG;
+  if (!(scale > 0.0f) || !(scale < 1e30f)) return CHAIN_ERR_ARG;
+  int64_t lse_sbh = 0;
+  if ((rc = lse_view(LSE, H, total, &lse_sbh))) return rc;
+  if (Hkv > 65535) return CHAIN_ERR_UNSUPPORTED;  // the V pre-pass grid's y extent
+  if (!workspace || !aligned16(workspace) ||
+      ws_bytes < attn_fwd_pv16_workspace((int)Hkv, (int)total, (int)d))
+    return CHAIN_ERR_ARG;
+  AttnFwdArgs args;
+  args.Q = Q->ptr; args.K = K->ptr; args.V = V->ptr; args.O = O->ptr;
+  args.q_sbh = Q->stride[1]; args.q_srow = Q->stride[0];
+  args.k_sbh = K->stride[1]; args.k_srow = K->stride[0];
+  args.v_sbh = V->stride[1]; args.v_srow = V->stride[0];
+  args.o_sbh = O->stride[1]; args.o_srow = O->stride[0];
+  args.LSE = static_cast<float *>(LSE->ptr); args.lse_sbh = lse_sbh;
+  args.BH = (int)H; args.BHkv = (int)Hkv; args.n = (int)total; args.d = (int)d;
+  args.causal = mask == CHAIN_MASK_CAUSAL; args.scale = scale;
+  args.n_loc = args.n;
+  args.q_sshard = args.k_sshard = args.v_sshard = args.o_sshard = 0;
+  args.cu_seqlens = cu_seqlens; args.nbatch = batch; args.max_seqlen = max_seqlen;
+  DevInfo *di = nullptr;
+  if ((rc = device_ready(&di))) return rc;
+  cudaError_t e = launch_attn_fwd_pv16(args, workspace, wait_cfg(di),
+                                       static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return CHAIN_ERR_UNSUPPORTED;
   return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
 }
 
@@ -692,6 +743,7 @@ int chain_bwd_varlen(const chain_tensor_t *dO, const chain_tensor_t *Q, const ch
   DevInfo *di = nullptr;
   if ((rc = device_ready(&di))) return rc;
   cudaError_t e = launch_attn_bwd(args, wait_cfg(di), static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return CHAIN_ERR_UNSUPPORTED;
   return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
 }
 

@@ -23,7 +23,7 @@ OFF_Q, OFF_K, OFF_V, OFF_DO = 0, 1, 2, 3
 class Workload:
     key: str
     index: int  # 1-based, fixes the seed base
-    kind: str  # "attn_fwd" | "mlp_fwd" | "relayout+attn_fwd" | "attn_bwd"
+    kind: str  # "attn_fwd" | "mlp_fwd" | "relayout+attn_fwd" | "attn_bwd" | "attn_fwd+attn_bwd"
     dims: dict = field(default_factory=dict)
 
     @property
@@ -50,7 +50,29 @@ WORKLOADS = {
     # to the nearest e4m3 value)
     "causal_attn_32k_e4m3": Workload("causal_attn_32k_e4m3", 6, "attn_fwd",
                                      dict(BH=32, n=32768, d=128, causal=True, dtype="e4m3")),
+    # grouped-query attention: 32 query heads over 8 K/V heads at n = 32768
+    "gqa_32k": Workload("gqa_32k", 7, "attn_fwd+attn_bwd",
+                        dict(BH=32, BHkv=8, n=32768, d=128, causal=True, dtype="bf16")),
+    # sequences of mixed lengths (see varlen_lengths) packed end to end into
+    # 131072 positions, 16 heads
+    "varlen_128k": Workload("varlen_128k", 8, "attn_fwd+attn_bwd",
+                            dict(total=131072, H=16, d=128, causal=True, dtype="bf16",
+                                 min_len=1024, max_len=16384)),
 }
+
+
+def varlen_lengths(total: int, min_len: int, max_len: int, seed: int):
+    """Sequence lengths drawn uniformly from [min_len, max_len] (seeded) until
+    they cover `total` positions; the last one is cut to fit."""
+    g = torch.Generator().manual_seed(int(seed))
+    lens = []
+    left = total
+    while left > 0:
+        n = int(torch.randint(min_len, max_len + 1, (1,), generator=g))
+        n = min(n, left)
+        lens.append(n)
+        left -= n
+    return lens
 
 
 def _gen(seed: int, device) -> torch.Generator:

@@ -264,7 +264,9 @@ int chain_fwd_sp_f16pv(const chain_tensor_t *Q, const chain_tensor_t *K,
  *               count from each sequence's start).
  *   LSE         [H][total] fp32, natural log.
  * Rows of each sequence are computed exactly as chain_fwd computes that
- * sequence alone.  Asynchronous on `stream`.
+ * sequence alone.  Returns CHAIN_ERR_UNSUPPORTED when H * batch *
+ * ceil(max_seqlen / 256) exceeds 2^31 - 1 (one thread block per head,
+ * sequence and pair of 128-row query tiles).  Asynchronous on `stream`.
  */
 int chain_fwd_varlen(const chain_tensor_t *Q, const chain_tensor_t *K,
                      const chain_tensor_t *V, const int32_t *cu_seqlens, int batch,
@@ -278,10 +280,14 @@ int chain_fwd_varlen(const chain_tensor_t *Q, const chain_tensor_t *K,
  *   K, V, dK, dV  [total][Hkv][d] bf16, one set of strides for the four
  *                 (grouped-query attention: dK, dV sum over each group);
  *   LSE           [H][total] fp32 as written by chain_fwd_varlen (dense);
- *   cu_seqlens, batch, max_seqlen, mask, scale as for chain_fwd_varlen.
+ *   cu_seqlens, batch, max_seqlen, mask, scale as for chain_fwd_varlen (a
+ *                 sequence longer than max_seqlen is not computed and the
+ *                 next chain_check() returns CHAIN_ERR_ARG).
  *   workspace     at least 4 * H * total bytes rounded up to 256, 16-byte
  *                 aligned (chain_bwd_workspace_size(Q, Q) returns it).
  * Each sequence's gradients are those chain_bwd gives for it alone.
+ * Returns CHAIN_ERR_UNSUPPORTED when H * batch * ceil(max_seqlen / 128)
+ * exceeds 2^31 - 1 (one thread block per head, sequence and 128-row tile).
  */
 int chain_bwd_varlen(const chain_tensor_t *dO, const chain_tensor_t *Q,
                      const chain_tensor_t *K, const chain_tensor_t *V,
@@ -317,6 +323,33 @@ size_t chain_fwd_f16pv_workspace_size(const chain_tensor_t *Q, const chain_tenso
 int chain_fwd_f16pv(const chain_tensor_t *Q, const chain_tensor_t *K,
                     const chain_tensor_t *V, int mask, float scale, chain_tensor_t *O,
                     chain_tensor_t *LSE, void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * chain_fwd_varlen_f16pv -- chain_fwd_varlen (sequences of different lengths
+ * packed end to end, each attending to itself only) with P V taken as one
+ * f16 product, as chain_fwd_f16pv does.
+ *   Q, K, V, O, LSE, cu_seqlens, batch, max_seqlen, mask, scale  as for
+ *               chain_fwd_varlen.
+ *   workspace  at least chain_fwd_varlen_f16pv_workspace_size(V) bytes,
+ *              16-byte aligned: V in f16, head-major [Hkv][total][d], and
+ *              one power-of-two scale per K/V head (taken over all of the
+ *              batch's rows of that head, as chain_fwd_f16pv takes it over
+ *              all of a head's rows).
+ * Error bound as for chain_fwd_f16pv.  LSE is bit for bit what
+ * chain_fwd_f16pv writes for each sequence alone, and so is O whenever no
+ * nonzero |v| of a head is below 2^-31 of that head's largest and the
+ * largest is at least 2^-80 (the per-head scale, a power of two, then
+ * changes no rounding).  Errors as chain_fwd_varlen,
+ * plus CHAIN_ERR_ARG for a missing or short workspace and
+ * CHAIN_ERR_UNSUPPORTED for more than 65,535 K/V heads;
+ * chain_fwd_varlen_f16pv_workspace_size returns 0 for a V it cannot take.
+ */
+size_t chain_fwd_varlen_f16pv_workspace_size(const chain_tensor_t *V);
+int chain_fwd_varlen_f16pv(const chain_tensor_t *Q, const chain_tensor_t *K,
+                           const chain_tensor_t *V, const int32_t *cu_seqlens, int batch,
+                           int max_seqlen, int mask, float scale, chain_tensor_t *O,
+                           chain_tensor_t *LSE, void *workspace, size_t ws_bytes,
+                           void *stream);
 
 /*
  * chain_fwd_fp8 -- softmax attention, O = softmax(scale Q K^T) (v_scale V),
