@@ -81,6 +81,9 @@ def _load():
             lib.chain_fwd_f16pv_workspace_size.argtypes = [P, P]
             lib.chain_fwd_sp_f16pv.argtypes = [P, P, P, ci, ci, ci, fl, P, P, vp, ctypes.c_size_t,
                                                vp]
+            lib.chain_fwd_f16h.argtypes = [P, P, P, ci, P, vp, ctypes.c_size_t, vp]
+            lib.chain_fwd_f16h_workspace_size.argtypes = [P]
+            lib.chain_fwd_f16h_workspace_size.restype = ctypes.c_size_t
             lib.chain_fwd_varlen_f16pv.argtypes = [P, P, P, vp, ci, ci, ci, fl, P, P, vp,
                                                    ctypes.c_size_t, vp]
             lib.chain_fwd_varlen_f16pv_workspace_size.argtypes = [P]
@@ -171,6 +174,18 @@ def chain_fwd(A, B, C, f, mask, scale, O, LSE=None, stream=None):
     _ok(_load().chain_fwd(_ref(desc(A)), _ref(desc(B)), _ref(desc(C)), int(f), int(mask),
                           float(scale), _ref(desc(O)), _ref(desc(LSE)), _stream(stream)),
         "chain_fwd")
+
+
+def chain_fwd_f16h(A, B, C, f, O, workspace, stream=None):
+    """MLP chain O = f(A B) C with the intermediate as one f16 tile; see include/chain.h."""
+    _ok(_load().chain_fwd_f16h(_ref(desc(A)), _ref(desc(B)), _ref(desc(C)), int(f), _ref(desc(O)),
+                               ctypes.c_void_p(workspace.data_ptr()),
+                               workspace.numel() * workspace.element_size(), _stream(stream)),
+        "chain_fwd_f16h")
+
+
+def chain_fwd_f16h_workspace_size(C) -> int:
+    return int(_load().chain_fwd_f16h_workspace_size(_ref(desc(C))))
 
 
 def chain_fwd_fp8(Q, K, V, mask, scale, v_scale, O, LSE, workspace, stream=None):
@@ -446,6 +461,16 @@ def attention_bwd(do, q, k, v, o, lse, causal: bool, scale: float | None = None,
     chain_bwd(do, q, k, v, o, lse, F_SOFTMAX, MASK_CAUSAL if causal else MASK_NONE, scale,
               dq, dk, dv, workspace, stream)
     return dq, dk, dv
+
+
+def mlp_chain_fwd_f16h(x, w1, w2, gelu: bool = True, workspace=None, stream=None):
+    """O = gelu_tanh(x w1) w2 (or (x w1) w2) with the intermediate as one f16 tile."""
+    o = torch.empty(x.shape[0], w2.shape[1], dtype=x.dtype, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(max(chain_fwd_f16h_workspace_size(w2), 16), dtype=torch.uint8,
+                                device=x.device)
+    chain_fwd_f16h(x, w1, w2, F_GELU_TANH if gelu else F_IDENTITY, o, workspace, stream)
+    return o
 
 
 def mlp_chain_fwd(x, w1, w2, gelu: bool = True, stream=None):

@@ -354,6 +354,46 @@ int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B, const chain_tens
   return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
 }
 
+size_t chain_fwd_f16h_workspace_size(const chain_tensor_t *C) {
+  View c;
+  if (view_of(C, 2, &c) || C->ndim != 2 || c.dtype != CHAIN_BF16) return 0;
+  if (c.rows < 1 || c.cols < 1 || c.rows > (1 << 30) || c.cols > (1 << 30)) return 0;
+  return mlp_f16h_workspace(c.rows, c.cols);
+}
+
+int chain_fwd_f16h(const chain_tensor_t *A, const chain_tensor_t *B, const chain_tensor_t *C,
+                   int f, chain_tensor_t *O, void *workspace, size_t ws_bytes, void *stream) {
+  if (f != CHAIN_F_IDENTITY && f != CHAIN_F_GELU_TANH) return CHAIN_ERR_ARG;
+  View a, b, c, o;
+  int rc;
+  if ((rc = view_of(A, 2, &a)) || (rc = view_of(B, 2, &b)) || (rc = view_of(C, 2, &c)) ||
+      (rc = view_of(O, 2, &o)))
+    return rc;
+  if (A->ndim != 2 || B->ndim != 2 || C->ndim != 2 || O->ndim != 2) return CHAIN_ERR_ARG;
+  if (a.dtype != CHAIN_BF16 || b.dtype != CHAIN_BF16 || c.dtype != CHAIN_BF16 ||
+      o.dtype != CHAIN_BF16)
+    return CHAIN_ERR_DTYPE;
+  if (a.cols != b.rows || b.cols != c.rows || o.rows != a.rows || o.cols != c.cols)
+    return CHAIN_ERR_ARG;
+  if (!pitch16(a) || !pitch16(b) || !pitch16(c) || !pitch16(o)) return CHAIN_ERR_ARG;
+  if (a.s_row != a.cols || b.s_row != b.cols || c.s_row != c.cols || o.s_row != o.cols)
+    return CHAIN_ERR_ARG;
+  MlpArgs m;
+  m.X = a.ptr; m.W1 = b.ptr; m.W2 = c.ptr; m.O = o.ptr;
+  m.M = (int)a.rows; m.K = (int)a.cols; m.N = (int)b.cols; m.P = (int)c.cols;
+  m.gelu = f == CHAIN_F_GELU_TANH;
+  if (m.M <= 0 || m.K <= 0 || m.N <= 0 || m.P <= 0) return CHAIN_ERR_ARG;
+  if (!workspace || !aligned16(workspace) || ws_bytes < mlp_f16h_workspace(m.N, m.P))
+    return CHAIN_ERR_ARG;
+  if (m.M % 128 || m.K % 64 || m.N % 64 || m.P % 256 || m.P < 512 || m.P > 1024)
+    return CHAIN_ERR_UNSUPPORTED;
+  DevInfo *di = nullptr;
+  if ((rc = device_ready(&di))) return rc;
+  cudaError_t e = launch_mlp_chain_f16h(m, workspace, wait_cfg(di), static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return CHAIN_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? CHAIN_OK : cuda_fail(e);
+}
+
 static size_t mlp_ws_bytes(const View &a, const View &c) {
   // H and dT, [M][N] bf16 each (M = rows of X, N = rows of W2)
   const size_t b = (size_t)a.rows * (size_t)c.rows * 2 * 2;

@@ -83,6 +83,12 @@ struct MlpArgs {
   int gelu;                 // 1 = gelu_tanh, 0 = identity
 };
 cudaError_t launch_mlp_chain(const MlpArgs &a, const WaitCfg &wc, cudaStream_t st);
+// The intermediate as one f16 tile against an f16 copy of W2 (in `ws`, at
+// least mlp_f16h_workspace(N, P) bytes); cluster shapes only (P = 512, 768
+// or 1024, N a multiple of 64), else cudaErrorNotSupported.
+size_t mlp_f16h_workspace(int64_t N, int64_t P);
+cudaError_t launch_mlp_chain_f16h(const MlpArgs &a, void *ws, const WaitCfg &wc,
+                                  cudaStream_t st);
 
 cudaError_t launch_relayout(const void *in, void *out, int64_t p, int64_t n_loc, int64_t H,
                             int64_t row_bytes, int64_t g, int inverse, cudaStream_t st);

@@ -370,7 +370,8 @@ constexpr int MAX_CS = 4;
 struct ClusterLayout {
   static constexpr int NST = 3;
   static constexpr uint32_t OFF_RING = 0;
-  static constexpr uint32_t OFF_SLOT = OFF_RING + NST * STAGE_BYTES;  // [MAX_CS] x (hi 16 KB, lo 16 KB)
+  // [MAX_CS] x 32 KB: (hi 16 KB, lo 16 KB), or the f16 H in the first 16 KB
+  static constexpr uint32_t OFF_SLOT = OFF_RING + NST * STAGE_BYTES;
   static constexpr uint32_t SLOT_BYTES = 32768;
   static constexpr uint32_t OFF_BAR = OFF_SLOT + MAX_CS * SLOT_BYTES;
   // full[3], empty[3], t_full[2], t_free[2], h_full[4], h_empty[4], o_done, mma_drain
@@ -382,14 +383,22 @@ struct ClusterLayout {
 struct ClusterParams {
   int M, K, N, P, gelu, CS;
   __nv_bfloat16 *O;
+  const float *w_inv;  // F16H: 2^-k undoing the scale of W2's f16 copy
   WaitCfg wc;
 };
 
+// F16H: the intermediate enters the second product as ONE f16 tile (11
+// significant bits) against an f16 copy of W2, instead of the bf16 pair
+// H_hi, H_lo against bf16 W2: one product per chunk instead of two, and half
+// the bytes per slot and per copy to the peers.
+template <bool F16H>
 __global__ void __launch_bounds__(NTHREADS, 1)
     mlp_cluster_kernel(const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmW1,
                        const __grid_constant__ CUtensorMap tmW2, const ClusterParams p) {
   using L = ClusterLayout;
+  // bytes of one hidden chunk in a slot: H_hi then H_lo, or the f16 H alone
+  constexpr uint32_t HBYTES = F16H ? L::SLOT_BYTES / 2 : L::SLOT_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -494,7 +503,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ------------------------------------------------------ MMA issuer
     {
       const uint32_t id1 = idesc_bf16_f32(BM, 2 * HC2, 0, 1);  // T = X W1 (a pair), W1 MN-major
-      const uint32_t id2 = idesc_bf16_f32(BM, BP, 0, 1);   // O += H W2, W2 MN-major
+      const uint32_t id2 = F16H ? idesc_f16_f32(BM, BP, 0, 1)     // O += H W2, W2 MN-major
+                                : idesc_bf16_f32(BM, BP, 0, 1);
       const uint32_t ring = smem_u32(smem + L::OFF_RING);
       int st = 0;
       bool ok = true;
@@ -527,7 +537,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (c % (2 * CS) == q && c + 2 * CS < NC && !(ok = gemm1(pair++))) break;
         // GEMM2 of chunk c from slot k = its owner
         const int k = c % CS, u = c / CS;
-        if (k != q && elect_one()) mbar_arrive_expect_tx(&h_full[k], L::SLOT_BYTES);
+        if (k != q && elect_one()) mbar_arrive_expect_tx(&h_full[k], HBYTES);
         __syncwarp();
         if (!mbar_wait_warp(&h_full[k], u & 1, p.wc, abort_flag, SITE_MLP_MMA)) {
           ok = false;
@@ -545,7 +555,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const SDesc dlo = sdesc_make(slot0 + k * L::SLOT_BYTES + 16384, 16, 1024);
         if (elect_one()) {
 #pragma unroll
-          for (int part = 0; part < 2; ++part)
+          for (int part = 0; part < (F16H ? 1 : 2); ++part)
 #pragma unroll
             for (int kk = 0; kk < HC2 / 16; ++kk)
               umma_f16_ss(tmem + 256, sdesc_at(part ? dlo : dhi, kk * 32), sdesc_at(bw, kk * 2048),
@@ -572,6 +582,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t my_hi = slot0 + q * L::SLOT_BYTES, my_lo = my_hi + 16384;
     const bool issuer = threadIdx.x == 0;
     bool ok = true;
+    bool beyond = false;  // F16H: some f(T) outside f16's finite range
     for (int i = 0; i < n_own; ++i) {
       const int j = i >> 1, h = i & 1, b = j & 1;  // pair j, half h, T buffer b
       if (ok && h == 0) ok = mbar_wait(&t_full[b], (j >> 1) & 1, p.wc, abort_flag, SITE_MLP_EPI);
@@ -591,9 +602,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           h0 = gelu_tanh(h0);
           h1 = gelu_tanh(h1);
         }
-        const uint32_t ph = pack_bf16(h0, h1);
-        hi[k / 2] = ph;
-        lo[k / 2] = pack_bf16(h0 - __uint_as_float(ph << 16), h1 - __uint_as_float(ph & 0xffff0000u));
+        if constexpr (F16H) {
+          const uint32_t ph = pack_f16(h0, h1);
+          hi[k / 2] = ph;
+          // an all-ones exponent field: infinite or NaN
+          beyond |= ((ph & 0x7c00u) == 0x7c00u) | ((ph & 0x7c000000u) == 0x7c000000u);
+        } else {
+          const uint32_t ph = pack_bf16(h0, h1);
+          hi[k / 2] = ph;
+          lo[k / 2] = pack_bf16(h0 - __uint_as_float(ph << 16), h1 - __uint_as_float(ph & 0xffff0000u));
+        }
       }
       // slot q may be overwritten once every CTA has run GEMM2 on the
       // previous own chunk and this CTA's copies of it have read the slot
@@ -607,7 +625,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int ch = 0; ch < 8; ++ch) {
         const uint32_t off = sw128_off(row, ch);
         st_shared_v4(my_hi + off, hi[4 * ch], hi[4 * ch + 1], hi[4 * ch + 2], hi[4 * ch + 3]);
-        st_shared_v4(my_lo + off, lo[4 * ch], lo[4 * ch + 1], lo[4 * ch + 2], lo[4 * ch + 3]);
+        if constexpr (!F16H)
+          st_shared_v4(my_lo + off, lo[4 * ch], lo[4 * ch + 1], lo[4 * ch + 2], lo[4 * ch + 3]);
       }
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
@@ -615,14 +634,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive(&h_full[q]);  // own GEMM2 reads the slot in place
         for (int r = 0; r < CS; ++r)
           if (r != q)
-            bulk_copy_to_cluster(mapa_shared(my_hi, (uint32_t)r), my_hi, L::SLOT_BYTES,
+            bulk_copy_to_cluster(mapa_shared(my_hi, (uint32_t)r), my_hi, HBYTES,
                                  mapa_shared(smem_u32(&h_full[q]), (uint32_t)r));
         bulk_commit_group();
       }
     }
+    if constexpr (F16H) {
+      // reported by the next chain_check (the result is then not valid)
+      if (__any_sync(0xffffffffu, beyond) && lane == 0) atomicExch(&p.wc.status->reserved[0], 1);
+    }
     // O epilogue
     if (ok && mbar_wait(o_done, 0, p.wc, abort_flag, SITE_MLP_EPI)) {
       tc_fence_after();
+      const float os = F16H ? __ldg(p.w_inv) : 1.0f;
       __nv_bfloat16 *orow = p.O + (int64_t)(rb * BM + row) * p.P + q * BP;
 #pragma unroll 1
       for (int j = 0; j < BP / 32; ++j) {
@@ -633,10 +657,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           uint4 o;
-          o.x = pack_bf16(__uint_as_float(r[8 * k + 0]), __uint_as_float(r[8 * k + 1]));
-          o.y = pack_bf16(__uint_as_float(r[8 * k + 2]), __uint_as_float(r[8 * k + 3]));
-          o.z = pack_bf16(__uint_as_float(r[8 * k + 4]), __uint_as_float(r[8 * k + 5]));
-          o.w = pack_bf16(__uint_as_float(r[8 * k + 6]), __uint_as_float(r[8 * k + 7]));
+          o.x = pack_bf16(__uint_as_float(r[8 * k + 0]) * os, __uint_as_float(r[8 * k + 1]) * os);
+          o.y = pack_bf16(__uint_as_float(r[8 * k + 2]) * os, __uint_as_float(r[8 * k + 3]) * os);
+          o.z = pack_bf16(__uint_as_float(r[8 * k + 4]) * os, __uint_as_float(r[8 * k + 5]) * os);
+          o.w = pack_bf16(__uint_as_float(r[8 * k + 6]) * os, __uint_as_float(r[8 * k + 7]) * os);
           dst[k] = o;
         }
       }
@@ -661,56 +685,156 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
+// ------------------------------------------------ W2 -> f16 (F16H only)
+// One power-of-two scale 2^k for the whole of W2, chosen from its largest
+// |w| (bf16 magnitude bits order like the values) so that it lands in
+// [2^14, 2^15): every bf16 value is then exact in f16 except values below
+// 2^-31 of that maximum (f16 subnormals, absolute error at most 2^-39 of
+// it).  Two passes: WPB partial maxima, then each block reduces them,
+// converts its share and (block 0) stores 2^-k for the epilogue.
+constexpr int WPB = 1024;  // blocks of both passes (partial maxima of the first)
+constexpr int WU = 4;      // 16-byte vectors in flight per thread and round
+
+__device__ __forceinline__ uint32_t block_max256(uint32_t v, uint32_t *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) v = max(v, red[w]);
+  __syncthreads();
+  return v;
+}
+
+__global__ void __launch_bounds__(256)
+    w_absmax_kernel(const uint4 *__restrict__ W, int64_t nvec, uint32_t *__restrict__ part) {
+  __shared__ uint32_t red[8];
+  const int64_t stride = (int64_t)gridDim.x * 256;
+  uint32_t m = 0;
+  for (int64_t base = blockIdx.x * 256 + threadIdx.x; base < nvec; base += WU * stride) {
+    uint4 x[WU];
+#pragma unroll
+    for (int u = 0; u < WU; ++u)
+      x[u] = base + u * stride < nvec ? __ldg(W + base + u * stride) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < WU; ++u) {
+      const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7fffu, (w[k] >> 16) & 0x7fffu));
+    }
+  }
+  m = block_max256(m, red);
+  if (threadIdx.x == 0) part[blockIdx.x] = m;
+}
+
+__global__ void __launch_bounds__(256)
+    w_to_f16_kernel(const uint4 *__restrict__ W, int64_t nvec, const uint32_t *__restrict__ part,
+                    uint4 *__restrict__ out, float *__restrict__ w_inv) {
+  __shared__ uint32_t red[8];
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < WPB / 256; ++i) m = max(m, part[i * 256 + threadIdx.x]);
+  m = block_max256(m, red);
+  // exponent field e of the largest |w|: k = 141 - e puts it in [2^14, 2^15);
+  // zero, infinite or NaN maxima keep k = 0
+  const int e = (int)(m >> 7);
+  int k = (m == 0 || e == 255) ? 0 : 141 - e;
+  k = k < -126 ? -126 : (k > 126 ? 126 : k);
+  const float sc = __uint_as_float((uint32_t)(127 + k) << 23);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *w_inv = __uint_as_float((uint32_t)(127 - k) << 23);
+  const int64_t stride = (int64_t)gridDim.x * 256;
+  for (int64_t base = blockIdx.x * 256 + threadIdx.x; base < nvec; base += WU * stride) {
+    uint4 x[WU];
+#pragma unroll
+    for (int u = 0; u < WU; ++u)
+      x[u] = base + u * stride < nvec ? __ldg(W + base + u * stride) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < WU; ++u) {
+      const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+      uint32_t y[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        y[q] = pack_f16(__uint_as_float(w[q] << 16) * sc, __uint_as_float(w[q] & 0xffff0000u) * sc);
+      if (base + u * stride < nvec) out[base + u * stride] = make_uint4(y[0], y[1], y[2], y[3]);
+    }
+  }
+}
+
+// Tensor maps of X [M][K] (64 x 128 boxes), W1 [K][N] and W2 [N][P] (64 x 64
+// boxes); W2 as bf16 or as its f16 copy.
+cudaError_t mlp_maps(const MlpArgs &a, const void *w2, CUtensorMapDataType w2_type,
+                     CUtensorMap *mx, CUtensorMap *mw1, CUtensorMap *mw2) {
+  cudaError_t e;
+  {
+    const uint64_t d[2] = {(uint64_t)a.K, (uint64_t)a.M};
+    const uint64_t s[1] = {(uint64_t)a.K * 2};
+    const uint32_t box[2] = {64, 128};
+    if ((e = make_tmap(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.X, d, s, box))) return e;
+  }
+  {
+    const uint64_t d[2] = {(uint64_t)a.N, (uint64_t)a.K};
+    const uint64_t s[1] = {(uint64_t)a.N * 2};
+    const uint32_t box[2] = {64, 64};
+    if ((e = make_tmap(mw1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.W1, d, s, box))) return e;
+  }
+  {
+    const uint64_t d[2] = {(uint64_t)a.P, (uint64_t)a.N};
+    const uint64_t s[1] = {(uint64_t)a.P * 2};
+    const uint32_t box[2] = {64, 64};
+    if ((e = make_tmap(mw2, w2_type, 2, w2, d, s, box))) return e;
+  }
+  return cudaSuccess;
+}
+
+template <bool F16H>
+cudaError_t launch_cluster(const MlpArgs &a, const CUtensorMap &mx, const CUtensorMap &mw1,
+                           const CUtensorMap &mw2, const float *w_inv, const WaitCfg &wc,
+                           cudaStream_t st) {
+  // X W1 once per row block, shared through the cluster
+  const int CS = a.P / BP;
+  ClusterParams p;
+  p.M = a.M; p.K = a.K; p.N = a.N; p.P = a.P; p.gelu = a.gelu; p.CS = CS;
+  p.O = static_cast<__nv_bfloat16 *>(a.O);
+  p.w_inv = w_inv;
+  p.wc = wc;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(mlp_cluster_kernel<F16H>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, ClusterLayout::ALLOC)))
+    return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((a.M / BM) * CS));
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = ClusterLayout::ALLOC;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, mlp_cluster_kernel<F16H>, mx, mw1, mw2, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+bool cluster_shape(const MlpArgs &a) {
+  const int CS = a.P / BP;
+  return a.P % BP == 0 && CS >= 2 && CS <= MAX_CS && a.N % HC2 == 0;
+}
+
 }  // namespace
 
 cudaError_t launch_mlp_chain(const MlpArgs &a, const WaitCfg &wc, cudaStream_t st) {
   if (a.M % BM || a.K % KT || a.N % HC || a.P % BP) return cudaErrorNotSupported;
   CUtensorMap mx, mw1, mw2;
   cudaError_t e;
-  {
-    const uint64_t d[2] = {(uint64_t)a.K, (uint64_t)a.M};
-    const uint64_t s[1] = {(uint64_t)a.K * 2};
-    const uint32_t box[2] = {64, 128};
-    if ((e = make_tmap(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.X, d, s, box))) return e;
-  }
-  {
-    const uint64_t d[2] = {(uint64_t)a.N, (uint64_t)a.K};
-    const uint64_t s[1] = {(uint64_t)a.N * 2};
-    const uint32_t box[2] = {64, 64};
-    if ((e = make_tmap(&mw1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.W1, d, s, box))) return e;
-  }
-  {
-    const uint64_t d[2] = {(uint64_t)a.P, (uint64_t)a.N};
-    const uint64_t s[1] = {(uint64_t)a.P * 2};
-    const uint32_t box[2] = {64, 64};
-    if ((e = make_tmap(&mw2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.W2, d, s, box))) return e;
-  }
-  const int CS = a.P / BP;
-  if (CS >= 2 && CS <= MAX_CS && a.N % HC2 == 0) {
-    // X W1 once per row block, shared through the cluster
-    ClusterParams p;
-    p.M = a.M; p.K = a.K; p.N = a.N; p.P = a.P; p.gelu = a.gelu; p.CS = CS;
-    p.O = static_cast<__nv_bfloat16 *>(a.O);
-    p.wc = wc;
-    if ((e = cudaFuncSetAttribute(mlp_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  ClusterLayout::ALLOC)))
-      return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((a.M / BM) * CS));
-    cfg.blockDim = dim3(NTHREADS);
-    cfg.dynamicSmemBytes = ClusterLayout::ALLOC;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)CS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+  if ((e = mlp_maps(a, a.W2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, &mx, &mw1, &mw2))) return e;
+  if (cluster_shape(a)) {
     timing_mark(st, 0);
-    e = cudaLaunchKernelEx(&cfg, mlp_cluster_kernel, mx, mw1, mw2, p);
+    e = launch_cluster<false>(a, mx, mw1, mw2, nullptr, wc, st);
     timing_mark(st, 1);
-    return e != cudaSuccess ? e : cudaGetLastError();
+    return e;
   }
   MlpParams p;
   p.M = a.M;
@@ -728,6 +852,33 @@ cudaError_t launch_mlp_chain(const MlpArgs &a, const WaitCfg &wc, cudaStream_t s
   mlp_chain_kernel<<<grid, NTHREADS, MlpLayout::ALLOC, st>>>(mx, mw1, mw2, p);
   timing_mark(st, 1);
   return cudaGetLastError();
+}
+
+size_t mlp_f16h_workspace(int64_t N, int64_t P) {
+  const size_t wb = ((size_t)N * (size_t)P * 2 + 255) & ~(size_t)255;
+  return wb + 4 * WPB + 256;
+}
+
+cudaError_t launch_mlp_chain_f16h(const MlpArgs &a, void *ws, const WaitCfg &wc,
+                                  cudaStream_t st) {
+  if (a.M % BM || a.K % KT || !cluster_shape(a)) return cudaErrorNotSupported;
+  uint8_t *base = static_cast<uint8_t *>(ws);
+  const size_t wb = ((size_t)a.N * (size_t)a.P * 2 + 255) & ~(size_t)255;
+  uint4 *w16 = reinterpret_cast<uint4 *>(base);
+  uint32_t *part = reinterpret_cast<uint32_t *>(base + wb);
+  float *w_inv = reinterpret_cast<float *>(base + wb + 4 * WPB);
+  const int64_t nvec = (int64_t)a.N * a.P / 8;  // P is a multiple of 256
+  timing_mark(st, 0);
+  w_absmax_kernel<<<WPB, 256, 0, st>>>(static_cast<const uint4 *>(a.W2), nvec, part);
+  w_to_f16_kernel<<<WPB, 256, 0, st>>>(static_cast<const uint4 *>(a.W2), nvec, part, w16, w_inv);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mx, mw1, mw2;
+  if ((e = mlp_maps(a, w16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, &mx, &mw1, &mw2))) return e;
+  timing_mark(st, 1);
+  e = launch_cluster<true>(a, mx, mw1, mw2, w_inv, wc, st);
+  timing_mark(st, 2);
+  return e;
 }
 
 }  // namespace chain

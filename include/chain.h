@@ -112,6 +112,37 @@ int chain_fwd(const chain_tensor_t *A, const chain_tensor_t *B,
               chain_tensor_t *O, chain_tensor_t *LSE, void *stream);
 
 /*
+ * chain_fwd_f16h -- the MLP chain O = f(A B) C of chain_fwd (f =
+ * CHAIN_F_GELU_TANH or CHAIN_F_IDENTITY; the unit of "Memory-efficient
+ * tensor parallelism", FITEE 10.1631/FITEE.2400602, abstract, with the
+ * intermediate kept on chip as the AutoSP write-up, section 2.B, requires),
+ * with the intermediate H = f(A B) entering the second product as ONE f16
+ * tile (11 significant bits) against an f16 copy of C, instead of the bf16
+ * pair H_hi + H_lo against bf16 C: one product per hidden chunk instead of
+ * two, and half the on-chip traffic of the intermediate.
+ *   A [M][K], B [K][N], C [N][P], O [M][P]: 2-D, row-major, contiguous
+ *   rows, bf16.  M a multiple of 128, K and N multiples of 64, P = 512, 768
+ *   or 1024 (the clusters of 2 to 4 thread blocks that share H), else
+ *   CHAIN_ERR_UNSUPPORTED.
+ *   workspace  at least chain_fwd_f16h_workspace_size(C) bytes, 16-byte
+ *              aligned: C in f16 (2 * N * P bytes) and its scale factor.
+ * The copy of C carries one power-of-two scale that puts its largest |c| in
+ * [2^14, 2^15); every value is then exact in f16 except values below 2^-31
+ * of that maximum (error at most 2^-39 of it).  The epilogue undoes the
+ * scale.  H must stay within f16's finite range (|H| <= 65504): a value
+ * beyond it is reported by the next chain_check() as CHAIN_ERR_ARG and the
+ * result is then not valid.  Values of |H| below 2^-14 are f16 subnormals
+ * (absolute error at most 2^-25).  Error otherwise: one bf16 rounding of O
+ * plus H's f16 rounding (~2^-12 relative, random over the hidden index).
+ * Returns CHAIN_ERR_DTYPE unless bf16, CHAIN_ERR_ARG for a shape, stride,
+ * alignment or workspace violation or another f.  Asynchronous on `stream`.
+ * chain_fwd_f16h_workspace_size returns 0 for an invalid C.
+ */
+size_t chain_fwd_f16h_workspace_size(const chain_tensor_t *C);
+int chain_fwd_f16h(const chain_tensor_t *A, const chain_tensor_t *B, const chain_tensor_t *C,
+                   int f, chain_tensor_t *O, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * chain_bwd_workspace_size -- bytes of device workspace chain_bwd needs for
  * these shapes, rounded up to 256 bytes.  A and C of one shape mean the
  * softmax chain: the fp32 [BH][n] row term D.  2-D A and C of different

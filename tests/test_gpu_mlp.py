@@ -69,3 +69,85 @@ def test_mlp_rejects_unsupported_shapes(cg):
     with pytest.raises(cg.ChainError) as ei:
         cg.mlp_chain_fwd(x, w1, w2)
     assert ei.value.status == cg.ERR_UNSUPPORTED
+
+
+# ------------------------------------------------- f16 intermediate (f16h)
+F16H_CASES = [(128, 64, 64, 512), (256, 128, 320, 768), (384, 192, 384, 1024), (256, 1024, 640, 768)]
+
+
+@pytest.mark.parametrize("gelu", [True, False])
+@pytest.mark.parametrize("M,K,N,P", F16H_CASES)
+def test_mlp_f16h_small_vs_oracle(cg, orc, M, K, N, P, gelu):
+    x, w1, w2 = cs.mlp_inputs(M, K, N, P, seed=2300 + M + K + N + P)
+    o = cg.mlp_chain_fwd_f16h(x.cuda(), w1.cuda(), w2.cuda(), gelu=gelu)
+    assert cg.chain_check()[0] == 0
+    ref = orc.chain_fwd(x, w1, w2, orc.F_GELU_TANH if gelu else orc.F_IDENTITY)
+    assert_fwd_close(o, ref, f"f16h {M}x{K}x{N}x{P} gelu={gelu}")
+
+
+def test_mlp_f16h_full_size_sampled(cg, orc):
+    wl = cs.WORKLOADS["gelu_mlp"]
+    dm = wl.dims
+    x, w1, w2 = cs.mlp_inputs(dm["M"], dm["K"], dm["N"], dm["P"], seed=wl.seed)
+    o = cg.mlp_chain_fwd_f16h(x.cuda(), w1.cuda(), w2.cuda(), gelu=True)
+    assert cg.chain_check()[0] == 0
+    g = torch.Generator().manual_seed(6)
+    rows = sorted(set([0, 1, 127, 128, dm["M"] - 1] + torch.randint(0, dm["M"], (123,), generator=g).tolist()))
+    ref = orc.chain_fwd(x, w1, w2, orc.F_GELU_TANH, rows=rows)
+    assert_fwd_close(o.cpu()[rows], ref, "f16h 4096 sampled")
+
+
+@pytest.mark.parametrize("w2_scale", [2.0 ** 30, 2.0 ** -40])
+def test_mlp_f16h_c_far_from_f16_range(cg, orc, w2_scale):
+    # C scaled far outside f16's range (2^30 x): its copy takes its own power
+    # of two, so the result stays within the forward bound
+    x, w1, w2 = cs.mlp_inputs(256, 128, 256, 512, seed=2400)
+    w2 = (w2.float() * w2_scale).to(torch.bfloat16)
+    o = cg.mlp_chain_fwd_f16h(x.cuda(), w1.cuda(), w2.cuda(), gelu=True)
+    assert cg.chain_check()[0] == 0
+    ref = orc.chain_fwd(x, w1, w2, orc.F_GELU_TANH)
+    assert_fwd_close(o, ref, f"f16h C x {w2_scale}")
+
+
+def test_mlp_f16h_matches_compensated_form(cg):
+    # the two forms of the same chain agree to within their rounding
+    x, w1, w2 = cs.mlp_inputs(512, 256, 512, 1024, seed=2500)
+    xd, w1d, w2d = x.cuda(), w1.cuda(), w2.cuda()
+    a = cg.mlp_chain_fwd_f16h(xd, w1d, w2d, gelu=True).float()
+    b = cg.mlp_chain_fwd(xd, w1d, w2d, gelu=True).float()
+    assert float((a - b).abs().max()) <= 1e-2 * float(b.abs().max())
+
+
+def test_mlp_f16h_intermediate_beyond_f16_is_reported(cg):
+    # X W1 of about 1e5: GeLU of it is beyond f16's largest finite value
+    x, w1, w2 = cs.mlp_inputs(128, 64, 64, 512, seed=2600)
+    x = torch.full_like(x, 64.0)
+    w1 = torch.full_like(w1, 32.0)  # T = 64 * 32 * 64 = 131072
+    cg.mlp_chain_fwd_f16h(x.cuda(), w1.cuda(), w2.cuda(), gelu=False)
+    rc, _ = cg.chain_check()
+    assert rc == cg.ERR_ARG
+    assert cg.chain_check()[0] == 0
+
+
+def test_mlp_f16h_rejects_bad_args(cg):
+    x = torch.zeros(128, 64, dtype=torch.bfloat16, device="cuda")
+    w1 = torch.zeros(64, 128, dtype=torch.bfloat16, device="cuda")
+    w2 = torch.zeros(128, 256, dtype=torch.bfloat16, device="cuda")  # P = 256: no cluster
+    with pytest.raises(cg.ChainError) as ei:
+        cg.mlp_chain_fwd_f16h(x, w1, w2)
+    assert ei.value.status == cg.ERR_UNSUPPORTED
+    w2 = torch.zeros(128, 512, dtype=torch.bfloat16, device="cuda")
+    need = cg.chain_fwd_f16h_workspace_size(w2)
+    assert need >= 128 * 512 * 2
+    o = torch.empty(128, 512, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(cg.ChainError) as ei:
+        cg.chain_fwd_f16h(x, w1, w2, cg.F_GELU_TANH, o,
+                          torch.empty(need - 16, dtype=torch.uint8, device="cuda"))
+    assert ei.value.status == cg.ERR_ARG
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    with pytest.raises(cg.ChainError) as ei:
+        cg.chain_fwd_f16h(x, w1, w2, cg.F_SOFTMAX, o, ws)
+    assert ei.value.status == cg.ERR_ARG
+    with pytest.raises(cg.ChainError) as ei:
+        cg.chain_fwd_f16h(x.float(), w1, w2, cg.F_GELU_TANH, o, ws)
+    assert ei.value.status == cg.ERR_DTYPE
