@@ -6,7 +6,7 @@
 //   dW2 = H^T dO,   dX = dT W1^T,   dW1 = X^T dT.
 //
 // Two kernels:
-//   mlp_bwd_act_kernel  one CTA per (128 rows, 128 hidden columns): T and dH
+//   mlp_bwd_act_kernel  one CTA per (128 rows, 256 hidden columns): T and dH
 //                       on the tensor cores (fp32 in tensor memory), then H
 //                       and dT as bf16 into the caller's workspace [M][N] x 2;
 //   gemm_kernel         the three products above as one launch of 128 x 256
@@ -55,9 +55,11 @@ __device__ __forceinline__ void gelu_tanh_and_grad(float t, float &g, float &dg)
 }
 
 // ------------------------------------------------------------ H and dT
+constexpr int HN = 256;  // hidden columns per CTA of the activation kernel
+
 struct ActLayout {
-  static constexpr int NSTAGE = 3;
-  static constexpr uint32_t STAGE = 32768;  // A tile 16 KB, B tile 16 KB
+  static constexpr int NSTAGE = 4;
+  static constexpr uint32_t STAGE = 16384 + HN * KT * 2;  // A tile 16 KB, B tile 32 KB
   static constexpr uint32_t OFF_BAR = NSTAGE * STAGE;
   static constexpr uint32_t NBAR = 2 * NSTAGE + 2;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nb = p.N / 128;
+  const int nb = p.N / HN;
   const int rb = blockIdx.x / nb, hb = blockIdx.x % nb;
   const int nk = p.K / KT, np = p.P / KT, nst = nk + np;
 
@@ -104,7 +106,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_barrier_init();
   }
   if (warp == 5) {
-    tmem_alloc(tmem_slot, 256);
+    tmem_alloc(tmem_slot, 2 * HN);
     tmem_relinquish();
   }
   if (warp == 4 && lane == 0) {
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // T [0,128), dH [128,256)
+  const uint32_t tmem = *tmem_slot;  // T [0,HN), dH [HN,2HN)
 
   if (warp == 4) {
     // -------------------------------------------------------- producer
@@ -131,12 +133,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive_expect_tx(&full[s], L::STAGE);
         if (st < nk) {  // X [rows][k tile] (K-major), W1 [k tile][hidden cols] (MN-major)
           tma_load_2d(dst, &tmX, &full[s], st * KT, rb * BM);
-          tma_load_2d(dst + 16384, &tmW1, &full[s], hb * 128, st * KT);
-          tma_load_2d(dst + 24576, &tmW1, &full[s], hb * 128 + 64, st * KT);
+#pragma unroll
+          for (int i = 0; i < HN / 64; ++i)
+            tma_load_2d(dst + 16384 + i * 8192, &tmW1, &full[s], hb * HN + i * 64, st * KT);
         } else {        // dO [rows][p tile] (K-major), W2 [hidden rows][p tile] (K-major)
           const int pt = st - nk;
           tma_load_2d(dst, &tmdO, &full[s], pt * KT, rb * BM);
-          tma_load_2d(dst + 16384, &tmW2, &full[s], pt * KT, hb * 128);
+#pragma unroll
+          for (int i = 0; i < HN / 128; ++i)
+            tma_load_2d(dst + 16384 + i * 16384, &tmW2, &full[s], pt * KT, hb * HN + i * 128);
         }
         issued = st + 1;
       }
@@ -151,8 +156,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // The whole warp runs the loop; one elected lane issues each group and
     // its commits.
     {
-      const uint32_t id_t = idesc_bf16_f32(BM, 128, 0, 1);   // T: W1 MN-major
-      const uint32_t id_h = idesc_bf16_f32(BM, 128, 0, 0);   // dH: W2 rows K-major
+      const uint32_t id_t = idesc_bf16_f32(BM, HN, 0, 1);   // T: W1 MN-major
+      const uint32_t id_h = idesc_bf16_f32(BM, HN, 0, 0);   // dH: W2 rows K-major
       bool ok = true;
       for (int st = 0; st < nst; ++st) {
         const int s = st % L::NSTAGE;
@@ -169,7 +174,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < KT / 16; ++kk)
-            umma_f16_ss(tmem + (is_t ? 0 : 128), sdesc_at(a, kk * 32),
+            umma_f16_ss(tmem + (is_t ? 0 : HN), sdesc_at(a, kk * 32),
                         sdesc_at(b, is_t ? kk * 2048 : kk * 32), is_t ? id_t : id_h,
                         (st > first || kk > 0) ? 1u : 0u);
           umma_commit(&empty[s]);
@@ -191,14 +196,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     if (mbar_wait(acc_full, 0, p.wc, abort_flag, SITE_MB_EPI)) {
       tc_fence_after();
-      const int64_t off = (int64_t)(rb * BM + row) * p.N + hb * 128;
+      const int64_t off = (int64_t)(rb * BM + row) * p.N + hb * HN;
       uint4 *hrow = reinterpret_cast<uint4 *>(p.H + off);
       uint4 *drow = reinterpret_cast<uint4 *>(p.dT + off);
 #pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < HN / 32; ++q) {
         uint32_t t[32], dh[32];
         tmem_ld32(tmem + lane_off + q * 32, t);
-        tmem_ld32(tmem + lane_off + 128 + q * 32, dh);
+        tmem_ld32(tmem + lane_off + HN + q * 32, dh);
         tmem_wait_ld();
         uint32_t hp[16], dp[16];
 #pragma unroll
@@ -225,7 +230,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   if (warp == 5) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 2 * HN);
   }
 }
 
@@ -447,7 +452,7 @@ cudaError_t launch_mlp_bwd(const MlpBwdArgs &a, const WaitCfg &wc, cudaStream_t 
     if ((e = cudaFuncSetAttribute(mlp_bwd_act_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   ActLayout::ALLOC)))
       return e;
-    const unsigned grid = (unsigned)((a.M / BM) * (a.N / 128));
+    const unsigned grid = (unsigned)((a.M / BM) * (a.N / HN));
     timing_mark(st, 0);
     mlp_bwd_act_kernel<<<grid, NTHREADS, ActLayout::ALLOC, st>>>(mx, mw1, mdo, mw2, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
