@@ -799,6 +799,27 @@ def measure_varlen(hp, reps=5):
         "timing": f"median of {reps} after 2 warm-ups; inputs larger than L2"}}
 
 
+def host_link_gbps(torch, dev, nbytes=1 << 30, reps=3):
+    """Pinned host <-> device copy bandwidth of this machine (best of reps,
+    one 1 GiB copy each way): the floor under the end-to-end figure."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+        best = None
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            dst.copy_(src, non_blocking=True)
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        out[name] = round(nbytes / (best * 1e-3) / 1e9, 1)
+    del h, d
+    return out
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -984,6 +1005,7 @@ def main():
 
         run(2)
         torch.cuda.synchronize()
+        link = host_link_gbps(torch, dev)
         barrier(dist)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -993,6 +1015,8 @@ def main():
         ms_e2e = max_over_ranks(e0.elapsed_time(e1), dist) / args.steps
         e2e = {"value": round(flops_all / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3),
+               "host_link_GBps": link,
+               "upload_floor_ms": round(h2d / (link["h2d"] * 1e9) * 1e3, 3),
                "overlap": "uploads and downloads on their own streams, double-buffered device sets; "
                           "each component waits for its own inputs only and returns its results "
                           "as soon as it has finished"}
