@@ -350,10 +350,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // One cluster of CS = P/256 CTAs (2 to 4) per 128-row block; CTA q of the
 // cluster owns output columns [256q, 256q+256).  The hidden dimension runs in
 // 64-wide chunks c.  Chunk c is computed (GEMM1, f, hi/lo split) once, by CTA
-// k = c % CS, into its slot k; CTA k then pushes the 32 KB H_hi/H_lo tile
-// into slot k of every other CTA with bulk copies.  Every CTA runs GEMM2 over
-// all chunks.  X W1 is formed once per row block instead of once per output
-// block.
+// k = c % CS, into its slot k; CTA k then pushes the 32 KB H_hi/H_lo tile (16
+// KB of f16 H in the F16H instance) into slot k of every other CTA with bulk
+// copies.  Every CTA runs GEMM2 over all chunks.  X W1 is formed once per row
+// block instead of once per output block.
 //
 // Slot k is written only by CTA k:
 //   h_full[k]   in every CTA: the chunk in slot k is present (remote: the
