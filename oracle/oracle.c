@@ -230,6 +230,14 @@ int oracle_softmax_fwd_blocked(int dtype, const void *Q, const void *K,
   return 0;
 }
 
+/* The stored elements [off, off + count) widened exactly to double. */
+static double *widen(const void *base, int dtype, int64_t off, int64_t count) {
+  double *w = (double *)malloc(sizeof(double) * (size_t)(count > 0 ? count : 1));
+  if (!w) return NULL;
+  for (int64_t t = 0; t < count; ++t) w[t] = elem(base, dtype, off + t);
+  return w;
+}
+
 /* ------------------------------------------------------------------------
  * Softmax attention backward by the textbook chain rule, without any
  * recompute trick (the GPU path recomputes S and P from the LSE, AutoSP 2.B;
@@ -258,70 +266,94 @@ int oracle_softmax_bwd(int dtype, const void *Q, const void *K, const void *V,
       i0 >= i1 || j0 < 0 || j1 > n || j0 >= j1)
     return -1;
   const int64_t nh = bh1 - bh0, nr = i1 - i0, nc = j1 - j0;
-  memset(dK, 0, sizeof(double) * (size_t)(nh * nc * d));
-  memset(dV, 0, sizeof(double) * (size_t)(nh * nc * dv));
-  int bad = 0;
-#pragma omp parallel
-  {
-    double *S = (double *)malloc(sizeof(double) * (size_t)n);
-    double *dP = (double *)malloc(sizeof(double) * (size_t)n);
-    double *pK = (double *)calloc((size_t)(nh * nc * d), sizeof(double));
-    double *pV = (double *)calloc((size_t)(nh * nc * dv), sizeof(double));
-    if (!S || !dP || !pK || !pV) {
+  /* the requested heads, widened to double once (exact) */
+  double *q = widen(Q, dtype, bh0 * n * d, nh * n * d);
+  double *k = widen(K, dtype, bh0 * n * d, nh * n * d);
+  double *v = widen(V, dtype, bh0 * n * dv, nh * n * dv);
+  double *g = widen(dO, dtype, bh0 * n * dv, nh * n * dv);
+  const int nt = oracle_num_threads();
+  double **pKt = (double **)calloc((size_t)nt, sizeof(double *));
+  double **pVt = (double **)calloc((size_t)nt, sizeof(double *));
+  int bad = !q || !k || !v || !g || !pKt || !pVt;
+  if (!bad) {
+#pragma omp parallel num_threads(nt)
+    {
+      int t = 0;
+#ifdef _OPENMP
+      t = omp_get_thread_num();
+#endif
+      double *S = (double *)malloc(sizeof(double) * (size_t)n);
+      double *dP = (double *)malloc(sizeof(double) * (size_t)n);
+      /* this thread's share of the dK, dV sums over rows */
+      double *pK = (double *)calloc((size_t)(nh * nc * d), sizeof(double));
+      double *pV = (double *)calloc((size_t)(nh * nc * dv), sizeof(double));
+      pKt[t] = pK;
+      pVt[t] = pV;
+      if (!S || !dP || !pK || !pV) {
 #pragma omp atomic write
-      bad = 1;
-    }
-#pragma omp for schedule(dynamic, 2) collapse(2)
-    for (int64_t h = 0; h < nh; ++h) {
-      for (int64_t r = 0; r < nr; ++r) {
-        if (!S || !dP || !pK || !pV) continue;
-        const int64_t bh = bh0 + h, i = i0 + r;
-        const int64_t nk = causal ? i + 1 : n;
-        const int64_t qo = (bh * n + i) * d, go = (bh * n + i) * dv;
-        double m = -INFINITY;
-        for (int64_t j = 0; j < nk; ++j) {
-          double acc = 0.0;
-          for (int64_t e = 0; e < d; ++e)
-            acc += elem(Q, dtype, qo + e) * elem(K, dtype, (bh * n + j) * d + e);
-          S[j] = scale * acc;
-          if (S[j] > m) m = S[j];
-          double g = 0.0;
-          for (int64_t e = 0; e < dv; ++e)
-            g += elem(dO, dtype, go + e) * elem(V, dtype, (bh * n + j) * dv + e);
-          dP[j] = g;
-        }
-        double l = 0.0;
-        for (int64_t j = 0; j < nk; ++j) l += exp(S[j] - m);
-        double Di = 0.0;
-        for (int64_t j = 0; j < nk; ++j) {
-          S[j] = exp(S[j] - m) / l; /* S now holds P */
-          Di += S[j] * dP[j];
-        }
-        D[h * nr + r] = Di;
-        double *dq = dQ + (h * nr + r) * d;
-        for (int64_t e = 0; e < d; ++e) dq[e] = 0.0;
-        for (int64_t j = 0; j < nk; ++j) {
-          const double ds = S[j] * (dP[j] - Di);
-          for (int64_t e = 0; e < d; ++e)
-            dq[e] += scale * ds * elem(K, dtype, (bh * n + j) * d + e);
-          if (j >= j0 && j < j1) {
-            double *kk = pK + (h * nc + (j - j0)) * d;
-            double *vv = pV + (h * nc + (j - j0)) * dv;
-            for (int64_t e = 0; e < d; ++e) kk[e] += scale * ds * elem(Q, dtype, qo + e);
-            for (int64_t e = 0; e < dv; ++e) vv[e] += S[j] * elem(dO, dtype, go + e);
+        bad = 1;
+      }
+      /* rows dealt round-robin: each thread's share of the row sums is the
+       * same on every run */
+#pragma omp for schedule(static, 1) collapse(2)
+      for (int64_t h = 0; h < nh; ++h) {
+        for (int64_t r = 0; r < nr; ++r) {
+          if (!S || !dP || !pK || !pV) continue;
+          const int64_t i = i0 + r;
+          const int64_t nk = causal ? i + 1 : n;
+          const double *qi = q + (h * n + i) * d, *gi = g + (h * n + i) * dv;
+          double m = -INFINITY;
+          for (int64_t j = 0; j < nk; ++j) {
+            const double *kj = k + (h * n + j) * d, *vj = v + (h * n + j) * dv;
+            double acc = 0.0;
+            for (int64_t e = 0; e < d; ++e) acc += qi[e] * kj[e];
+            S[j] = scale * acc;
+            if (S[j] > m) m = S[j];
+            double gv = 0.0;
+            for (int64_t e = 0; e < dv; ++e) gv += gi[e] * vj[e];
+            dP[j] = gv;
+          }
+          double l = 0.0;
+          for (int64_t j = 0; j < nk; ++j) l += exp(S[j] - m);
+          double Di = 0.0;
+          for (int64_t j = 0; j < nk; ++j) {
+            S[j] = exp(S[j] - m) / l; /* S now holds P */
+            Di += S[j] * dP[j];
+          }
+          D[h * nr + r] = Di;
+          double *dq = dQ + (h * nr + r) * d;
+          for (int64_t e = 0; e < d; ++e) dq[e] = 0.0;
+          for (int64_t j = 0; j < nk; ++j) {
+            const double ds = S[j] * (dP[j] - Di);
+            const double *kj = k + (h * n + j) * d;
+            for (int64_t e = 0; e < d; ++e) dq[e] += scale * ds * kj[e];
+            if (j >= j0 && j < j1) {
+              double *kk = pK + (h * nc + (j - j0)) * d;
+              double *vv = pV + (h * nc + (j - j0)) * dv;
+              for (int64_t e = 0; e < d; ++e) kk[e] += scale * ds * qi[e];
+              for (int64_t e = 0; e < dv; ++e) vv[e] += S[j] * gi[e];
+            }
           }
         }
       }
+      free(S);
+      free(dP);
     }
-#pragma omp critical
-    {
-      if (pK && pV) {
-        for (int64_t t = 0; t < nh * nc * d; ++t) dK[t] += pK[t];
-        for (int64_t t = 0; t < nh * nc * dv; ++t) dV[t] += pV[t];
-      }
-    }
-    free(S); free(dP); free(pK); free(pV);
   }
+  /* dK, dV: the threads' shares added in thread order (deterministic) */
+  memset(dK, 0, sizeof(double) * (size_t)(nh * nc * d));
+  memset(dV, 0, sizeof(double) * (size_t)(nh * nc * dv));
+  for (int t = 0; t < nt && !bad; ++t) {
+    if (!pKt[t] || !pVt[t]) continue; /* a thread that ran no iteration */
+    for (int64_t u = 0; u < nh * nc * d; ++u) dK[u] += pKt[t][u];
+    for (int64_t u = 0; u < nh * nc * dv; ++u) dV[u] += pVt[t][u];
+  }
+  for (int t = 0; t < nt && pKt && pVt; ++t) {
+    free(pKt[t]);
+    free(pVt[t]);
+  }
+  free(pKt); free(pVt);
+  free(q); free(k); free(v); free(g);
   return bad ? -3 : 0;
 }
 
