@@ -35,7 +35,9 @@ extern "C" int chain_bwd_noalloc(const chain_tensor_t *dO, const chain_tensor_t 
                                  int mask, float scale, chain_tensor_t *dA, chain_tensor_t *dB,
                                  chain_tensor_t *dC, void *stream) {
   using namespace chain;
-  const size_t need = chain_bwd_workspace_size(A, C);
+  // Sized by the chain f names: an MLP whose X and W2 share one shape would
+  // otherwise be sized as attention.
+  const size_t need = chain_bwd_workspace_size_f(A, C, f);
   if (need == 0) return CHAIN_ERR_ARG;
   if (need > CHAIN_NOALLOC_SCRATCH_BYTES) return CHAIN_ERR_SCRATCH_LIMIT;
   int dev = 0;
@@ -55,9 +57,10 @@ extern "C" int chain_bwd_noalloc(const chain_tensor_t *dO, const chain_tensor_t 
     }
     scratch = g_noalloc_addr[dev];
   }
-  // Same checks and kernels as chain_bwd; the preprocess kernel rewrites D
-  // for every row on every call, so what an earlier call left in the array
-  // is never read.
+  // Same checks and kernels as chain_bwd.  Every call rewrites what it
+  // later reads (D for every query row of the attention backward; H and dT
+  // of every row of the MLP backward), so what an earlier call left in the
+  // array is never read.
   return chain_bwd(dO, A, B, C, O, LSE, f, mask, scale, dA, dB, dC, scratch,
                    CHAIN_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -530,7 +530,7 @@ static int relayout_common(const chain_tensor_t *seq, const chain_tensor_t *hm, 
     return CHAIN_ERR_ARG;
   const int64_t row_bytes = d * esize(seq->dtype);
   if (row_bytes % 16 || !aligned16(seq->ptr) || !aligned16(hm->ptr)) return CHAIN_ERR_ARG;
-  if (p * n_loc * H * (row_bytes / 16) >= (int64_t(1) << 32)) return CHAIN_ERR_ARG;
+  if (!relayout_fits_32bit(p * n_loc * H * (row_bytes / 16))) return CHAIN_ERR_ARG;
   DevInfo *di = nullptr;
   int rc = device_ready(&di);
   if (rc) return rc;

@@ -92,6 +92,16 @@ cudaError_t launch_mlp_chain_f16h(const MlpArgs &a, void *ws, const WaitCfg &wc,
 
 cudaError_t launch_relayout(const void *in, void *out, int64_t p, int64_t n_loc, int64_t H,
                             int64_t row_bytes, int64_t g, int inverse, cudaStream_t st);
+// The relayout kernel indexes 16-byte vectors in 32 bits with a grid-stride
+// loop of at most kRelayoutMaxGrid blocks x 256 threads x 4 vectors per step.
+// Its counter may run one whole step past the last vector before the loop
+// ends, so the sequence-major side's vector count plus one step must stay
+// below 2^32 (checked before launch).
+constexpr int64_t kRelayoutMaxGrid = 4096;
+constexpr int64_t kRelayoutStepVectors = kRelayoutMaxGrid * 256 * 4;
+inline bool relayout_fits_32bit(int64_t seq_vectors) {
+  return seq_vectors > 0 && seq_vectors + kRelayoutStepVectors < (int64_t(1) << 32);
+}
 
 // Keeps `e` as the thread's last CUDA error and returns CHAIN_ERR_CUDA.
 int record_cuda_error(cudaError_t e);

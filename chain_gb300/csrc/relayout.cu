@@ -63,14 +63,16 @@ cudaError_t launch_relayout(const void *in, void *out, int64_t p, int64_t n_loc,
   const int64_t N = p * n_loc;
   const int64_t vrow = row_bytes / 16;
   const int64_t total = N * Hl * vrow;
-  // 32-bit index arithmetic covers both sides: the sequence-major side has
-  // N*H*vrow vectors.
-  if (N * H * vrow >= (int64_t(1) << 32) || total == 0) return cudaErrorInvalidValue;
+  // 32-bit index arithmetic covers both sides (the sequence-major side has
+  // N*H*vrow vectors), with room for the loop counter's last step.
+  static_assert(THREADS * UNROLL * kRelayoutMaxGrid == kRelayoutStepVectors, "step size");
+  if (!relayout_fits_32bit(N * H * vrow) || total == 0) return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int64_t want = (total + (int64_t)THREADS * UNROLL - 1) / ((int64_t)THREADS * UNROLL);
-  const int64_t cap = (int64_t)(sms > 0 ? sms : 152) * 8;
+  int64_t cap = (int64_t)(sms > 0 ? sms : 152) * 8;
+  if (cap > kRelayoutMaxGrid) cap = kRelayoutMaxGrid;
   const unsigned grid = (unsigned)(want < cap ? want : cap);
   timing_mark(st, 0);
   relayout_kernel<<<grid, THREADS, 0, st>>>(

@@ -37,6 +37,11 @@
  *  - Thread safety: calls may be issued concurrently from several host
  *    threads; the only global state is a per-device cache of attributes
  *    guarded by a mutex.
+ *  - Device resets: the per-device cache holds device addresses of the
+ *    library's own status word (and of chain_bwd_noalloc's scratch array),
+ *    looked up on the first call on each device.  A device reset
+ *    (cudaDeviceReset) makes them stale: do not call the library on a device
+ *    after resetting it in the same process.
  */
 #ifndef CHAIN_GB300_H
 #define CHAIN_GB300_H
@@ -210,12 +215,18 @@ int chain_bwd(const chain_tensor_t *dO, const chain_tensor_t *A,
  * memory that every GPU which loads the library holds until the process
  * exits.  It never calls cudaMalloc, cudaFree or any allocating routine.
  *
- * Limit: chain_bwd_workspace_size(A, C) must not exceed
- * CHAIN_NOALLOC_SCRATCH_BYTES (BH * n <= 8,388,608 rows), else the call
- * returns CHAIN_ERR_SCRATCH_LIMIT before enqueuing anything.
+ * Limit: chain_bwd_workspace_size_f(A, C, f) must not exceed
+ * CHAIN_NOALLOC_SCRATCH_BYTES, else the call returns CHAIN_ERR_SCRATCH_LIMIT
+ * before enqueuing anything.  For the attention backward that is
+ * BH * n <= 8,388,608 query rows (4 bytes each); for the MLP backward
+ * M * N <= 8,388,608 elements of X W1 (H and dT, 2 bytes each), e.g. M = 2048
+ * rows at N = 4096 hidden units.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture begins.
+ * before any stream capture begins.  The address is kept for the life of the
+ * process: after a device reset (cudaDeviceReset) the array is a new one and
+ * the kept address is stale, so like the rest of this library (see
+ * "Device resets" above) this entry point must not be called after a reset.
  * All calls on a device share the one array and leave their partial
  * results in it; each call re-initialises what it reads.  Calls whose
  * execution overlaps on the GPU (different streams, or host threads without
@@ -421,6 +432,9 @@ int chain_fwd_fp8(const chain_tensor_t *Q, const chain_tensor_t *K,
  *   out    [H/p][p*n_loc][d]: out[h][s*n_loc+t][e] = shards[s][t][g*H/p+h][e]
  *   with g = head_group in [0, p).  Bit-exact copy of any 1-, 2- or 4-byte
  *   element type; d * element size must be a multiple of 16 bytes.
+ *   Size limit: the shards may hold at most 2^32 - 2^22 - 1 16-byte vectors
+ *   (p * n_loc * H * d * element size / 16; 64 GiB less 64 MiB), else
+ *   CHAIN_ERR_ARG before anything is enqueued.
  */
 int sp_relayout(const chain_tensor_t *shards, int p, int head_group,
                 chain_tensor_t *out, void *stream);
@@ -429,7 +443,7 @@ int sp_relayout(const chain_tensor_t *shards, int p, int head_group,
  * sp_relayout_inverse -- head-major -> sequence shards (the second
  * exchange of the Ulysses layer, "Analyse et Implications"):
  *   shards[s][t][g*H/p+h][e] = in[h][s*n_loc+t][e]; the other heads of
- *   `shards` are left untouched.  Same element and alignment rules.
+ *   `shards` are left untouched.  Same element, alignment and size rules.
  */
 int sp_relayout_inverse(const chain_tensor_t *in, int p, int head_group,
                         chain_tensor_t *shards, void *stream);

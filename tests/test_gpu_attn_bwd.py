@@ -66,6 +66,13 @@ def test_bwd_causal_64k_full_size(cg, orc):
             rq, _, _, _ = orc.softmax_bwd(q, k, v, do, scale, True, heads=(h, h + 1),
                                           row_range=(a, a + 64), col_range=(a, a + 1))
             assert_grad_close(dq[h, a:a + 64], rq[0], f"dQ rows {a} head {h}")
+    # key block 0 of head 0 in full: every one of the n queries attends to
+    # it, so the dK/dV kernel accumulates it over all n/128 query tiles.
+    rq, rk, rv, _ = orc.softmax_bwd(q, k, v, do, scale, True, heads=(0, 1),
+                                    row_range=(0, n), col_range=(0, 128))
+    assert_grad_close(dk[0, :128], rk[0], "dK key block 0 head 0")
+    assert_grad_close(dv[0, :128], rv[0], "dV key block 0 head 0")
+    assert_grad_close(dq[0], rq[0], "dQ head 0, every row")
     # invariants over every tile of every head: the key-sum of dK vanishes,
     # the key-sum of dV equals the query-sum of dO.
     dk64 = dk.double()
@@ -105,3 +112,20 @@ def test_bwd_grouped_query_vs_oracle(cg, orc, BH, BHkv, n, d, causal):
     assert_grad_close(dq, rq, "GQA dQ")
     assert_grad_close(dk, rk, "GQA dK")
     assert_grad_close(dv, rv, "GQA dV")
+
+
+def test_bwd_causal_16k_one_head_complete(cg, orc):
+    # One causal head at n = 16384, d = 128: every element of dQ, dK and dV
+    # against the oracle (128 query tiles, 128 key blocks).
+    q, k, v, do = cs.attn_inputs(1, 16384, 128, seed=9400, with_do=True)
+    scale = 128 ** -0.5
+    dq, dk, dv = run_bwd(cg, q, k, v, do, True, scale)
+    rq, rk, rv, _ = orc.softmax_bwd(q, k, v, do, scale, True)
+    assert_grad_close(dq, rq, "dQ n=16384")
+    assert_grad_close(dk, rk, "dK n=16384")
+    assert_grad_close(dv, rv, "dV n=16384")
+    # and per key block, so an error confined to one block is not averaged away
+    for j in range(0, 16384, 128):
+        assert_grad_close(dk[0, j:j + 128], rk[0, j:j + 128], f"dK block {j // 128}")
+        assert_grad_close(dv[0, j:j + 128], rv[0, j:j + 128], f"dV block {j // 128}")
+        assert_grad_close(dq[0, j:j + 128], rq[0, j:j + 128], f"dQ tile {j // 128}")

@@ -169,3 +169,60 @@ def test_sp_f16pv_full_size_matches_unfused(cg):
     ro, rl = _unfused_f16pv(cg, q, k, v, p, 0, True, d ** -0.5, o_init)
     assert torch.equal(o.view(torch.int16), ro.view(torch.int16))
     assert torch.equal(lse.view(torch.int32), rl.view(torch.int32))
+
+
+# --------------------- the Ulysses workload at full size against the oracle
+def _ulysses_rows(Hl, n, seed):
+    """(head, row) pairs: per head rows 0, 1, 127, 128, n-2, n-1, three rows
+    of the last 256-query block (whose causal rows span every key tile) and
+    seeded rows elsewhere, at least 16 per head."""
+    g = np.random.default_rng(seed)
+    out = []
+    for h in range(Hl):
+        fixed = {0, 1, 127, 128, n - 2, n - 1}
+        fixed |= set(int(r) for r in g.integers(n - 256, n, 3))
+        fixed |= set(int(r) for r in g.integers(0, n, 12))
+        out.extend((h, r) for r in sorted(fixed))
+    return np.asarray(out, dtype=np.int64)
+
+
+def test_ulysses_128k_full_size_vs_oracle(cg, orc):
+    # The Ulysses workload as the benchmark runs it: shards 4 x [32768][32][128]
+    # bf16 ~ N(0,1) (seeds of the workload), head group 0 relayouted to
+    # [8][131072][128], causal attention on those heads through
+    # chain_fwd_f16pv; then the same heads straight from the shards through
+    # chain_fwd_sp_f16pv and chain_fwd_sp.  The oracle attends the heads its
+    # own relayout produced, on sampled rows.
+    wl = cs.WORKLOADS["ulysses_128k"]
+    dm = wl.dims
+    p, n_loc, H, d, g = dm["p"], dm["n_loc"], dm["H"], dm["d"], dm["g"]
+    Hl, n = H // p, p * n_loc
+    scale = d ** -0.5
+    shards = [cs.shard_inputs(p, n_loc, H, d, seed=wl.seed + t) for t in range(3)]
+    heads = []
+    for x in shards:
+        raw, shape = orc.relayout(x, p, g)
+        heads.append(torch.from_numpy(raw).view(torch.bfloat16).reshape(shape))
+    rows = _ulysses_rows(Hl, n, seed=41)
+    ro, rl = orc.softmax_fwd(heads[0], heads[1], heads[2], scale, True, rows=rows)
+
+    def check(o_hm, lse, what):
+        o_hm, lse = o_hm.cpu(), lse.cpu()
+        assert_fwd_close(o_hm[rows[:, 0], rows[:, 1]], ro, f"{what} sampled O")
+        assert_lse_close(lse[rows[:, 0], rows[:, 1]], rl, f"{what} sampled LSE")
+
+    sd = [x.cuda() for x in shards]
+    # the step's calls: sp_relayout of Q, K, V, then chain_fwd_f16pv
+    hm = [cg.relayout(x, p, g) for x in sd]
+    o, lse = cg.attention_fwd_f16pv(hm[0], hm[1], hm[2], True, scale)
+    assert cg.chain_check()[0] == 0
+    check(o, lse, "relayout + chain_fwd_f16pv")
+    del hm, o
+    # fused: read from and written back to the shards
+    for name, fn in (("chain_fwd_sp_f16pv", cg.attention_fwd_sp_f16pv),
+                     ("chain_fwd_sp", cg.attention_fwd_sp)):
+        o_sh, lse = fn(sd[0], sd[1], sd[2], p, g, True, scale)
+        assert cg.chain_check()[0] == 0
+        raw, shape = orc.relayout(o_sh.cpu(), p, g)
+        check(torch.from_numpy(raw).view(torch.bfloat16).reshape(shape), lse, name)
+        del o_sh

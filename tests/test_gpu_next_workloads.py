@@ -56,6 +56,17 @@ def test_gqa_32q8kv_full_size(cg, orc):
                 assert_grad_close(dq[h, i0:], rq[0], f"GQA dQ tail head {h}")
         assert_grad_close(dk[hkv, i0:], sk, f"GQA dK tail K/V head {hkv}")
         assert_grad_close(dv[hkv, i0:], sv, f"GQA dV tail K/V head {hkv}")
+    # key block 0 of K/V head 0 in full: the dK/dV kernel accumulates it over
+    # every query tile of all G query heads of the group
+    sk = np.zeros((128, d))
+    sv = np.zeros((128, d))
+    for h in range(G):
+        _, rk, rv, _ = orc.softmax_bwd(q, kr, vr, do, scale, True, heads=(h, h + 1),
+                                       row_range=(0, n), col_range=(0, 128))
+        sk += rk[0]
+        sv += rv[0]
+    assert_grad_close(dk[0, :128], sk, "GQA dK key block 0, K/V head 0")
+    assert_grad_close(dv[0, :128], sv, "GQA dV key block 0, K/V head 0")
     # over every K/V head: the key-sum of dK vanishes; the key-sum of dV
     # equals the query-sum of its group's dO
     dk64 = dk.double()
