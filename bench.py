@@ -510,6 +510,41 @@ def measure_sp_fused(hp, reps=5):
         "timing": f"median of {reps} after 2 warm-ups; inputs larger than L2"}}
 
 
+def measure_relayout_clean(hp, reps=7):
+    """sp_relayout of the Q, K and V shards, each launch preceded by a read of
+    a 512 MB buffer, so that L2 holds no dirty lines of an earlier kernel when
+    it starts.  Inside the step, a relayout that follows a kernel which wrote
+    a lot (the previous relayout, the backward) also writes those lines back
+    to DRAM during its own launch; this row measures the kernel alone."""
+    torch, cg = hp.torch, hp.cg
+    u = hp.u
+    Hl, N = u["H"] // u["p"], u["p"] * u["n_loc"]
+    nbytes = 2.0 * Hl * N * u["d"] * 2
+    big = torch.empty(256 * 1024 * 1024, dtype=torch.float16, device=hp.dev)  # 512 MB, > L2
+    big.fill_(1.0)
+    ts = {t: [] for t in range(3)}
+    for _ in range(reps):
+        for t in range(3):
+            big.sum()
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            cg.set_timing_events(*evs)
+            cg.sp_relayout(hp.shards[t], u["p"], u["g"], hp.hm[t])
+            cg.set_timing_events()
+            torch.cuda.synchronize()
+            ts[t].append(evs[0].elapsed_time(evs[1]))
+    peaks, _ = load_peaks()
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    out = {}
+    for t in range(3):
+        ms = statistics.median(ts[t])
+        gb = nbytes / (ms * 1e-3) / 1e9
+        out["QKV"[t]] = {"ms": round(ms, 4), "GBps": round(gb, 1),
+                         "frac_of_measured_hbm": round(gb / hbm, 4), "frac_of_8TBps": round(gb / 8000.0, 4)}
+    del big
+    return {"sp_relayout_after_clean_l2": dict(out, timing=f"median of {reps}; each launch after a "
+                                                             "512 MB read (L2 without dirty lines)")}
+
+
 def measure_mlp_bwd(hp, reps=10):
     """Backward of the GeLU MLP workload (intermediate recomputed): the
     activation kernel and the batched product kernel, timed at their
@@ -1090,6 +1125,8 @@ def main():
     nxt = {}
     if hp.shards[0].numel() and (args.only is None or "sp" in args.only):
         nxt.update(measure_sp_fused(hp))
+    if hp.shards[0].numel() and (args.only is None or "relayout" in args.only):
+        nxt.update(measure_relayout_clean(hp))
     if hp.mlp_ok:
         nxt.update(measure_mlp_bwd(hp))
         nxt.update(measure_mlp_compensated(hp))
