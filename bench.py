@@ -1090,6 +1090,16 @@ def main():
                 hp.comp[c]["name"]: round(statistics.mean(wait(k, c) for k in steps), 3)
                 for c in range(ncomp)}
             out["host_issue_ms"] = round(statistics.mean(trace[k]["host_ms"] for k in steps), 3)
+            # one steady-state step in absolute terms: per component, when its
+            # upload, compute and download ran (ms from that step's first
+            # upload), to show which stream a slow step waited on
+            k = len(trace) - 2 if len(trace) >= 3 else len(trace) - 1
+            z = trace[k]["up"][0][0]
+            out["step_detail_ms"] = {
+                hp.comp[c]["name"]: [round(el(z, e), 2) for n_ in ("up", "comp", "down")
+                                     for e in trace[k][n_][c]]
+                for c in range(ncomp)}
+            out["step_detail_fields"] = "up start, up end, compute start, compute end, down start, down end"
             return out
 
         run(2)
