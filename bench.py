@@ -318,11 +318,16 @@ class HotPath:
 
     def step(self, events=None):
         """One pass over every component; events[i] (len(kernels) + 1 CUDA
-        events) are recorded at the main-kernel boundaries of component i."""
+        events) are recorded at the main-kernel boundaries of component i.
+        Each component runs inside an NVTX range of its name, so a profiler's
+        timeline shows the step's structure."""
+        nvtx = self.torch.cuda.nvtx
         for i, c in enumerate(self.comp):
             if events is not None:
                 self.cg.set_timing_events(*events[i])
+            nvtx.range_push(c["name"])
             c["fn"]()
+            nvtx.range_pop()
         if events is not None:
             self.cg.set_timing_events()
 
