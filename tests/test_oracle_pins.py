@@ -227,6 +227,23 @@ def test_bwd_row_and_column_ranges(orc):
     assert rel(dVp, dV[1:3, i0:]) < 1e-12
 
 
+def test_bwd_repeatable_and_key_block_of_full_rows(orc):
+    # Repeated calls give identical bits (each thread's share of the dK, dV
+    # row sums is fixed and the shares are added in thread order), and a key
+    # block taken over every row equals the same block of the full gradient:
+    # the form the full-length parity tests use.
+    n = 300
+    Q, K, V, G = cs.attn_inputs(2, n, 16, seed=63, dtype=torch.bfloat16, with_do=True)
+    a = orc.softmax_bwd(Q, K, V, G, 0.25, True, heads=(1, 2), row_range=(0, n), col_range=(0, 128))
+    b = orc.softmax_bwd(Q, K, V, G, 0.25, True, heads=(1, 2), row_range=(0, n), col_range=(0, 128))
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    dQ, dK, dV, _ = orc.softmax_bwd(Q, K, V, G, 0.25, True)
+    assert rel(a[0], dQ[1:2]) < 1e-14
+    assert rel(a[1], dK[1:2, :128]) < 1e-12
+    assert rel(a[2], dV[1:2, :128]) < 1e-12
+
+
 # --------------------------------------------------------------------- chain
 def test_identity_chain_associativity(orc):
     A, B, C = (np.random.default_rng(s).standard_normal(sh)
