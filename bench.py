@@ -427,7 +427,33 @@ def oracle_sample(scale: int = 3):
     f = len(rows) * (2.0 * m["K"] * m["N"] + 2.0 * m["N"] * m["P"])
     flops, secs = flops + f, secs + dt
     parts.append(f"GeLU MLP {len(rows)} rows of 4096 ({dt:.1f}s)")
+    # the fp32 attention of the tiny workload, in full
+    c1 = W["tiny_attn_fp32"].dims
+    q, k, v = cs.attn_inputs(c1["BH"], c1["n"], c1["d"], seed=W["tiny_attn_fp32"].seed,
+                             dtype=torch.float32)
+    t0 = time.perf_counter()
+    oracle.softmax_fwd(q, k, v, c1["d"] ** -0.5, False)
+    dt = time.perf_counter() - t0
+    f = 4.0 * c1["BH"] * c1["n"] * c1["n"] * c1["d"]
+    flops, secs = flops + f, secs + dt
+    parts.append(f"fp32 attention 1x256x64 in full ({dt:.3f}s)")
     return flops / secs / 1e12, secs, "; ".join(parts), oracle.num_threads()
+
+
+def oracle_relayout_gbps():
+    """The oracle's relayout of one full Ulysses tensor (4 x [32768][32][128] bf16 shards to
+    the 8 heads of group 0): bytes read plus written per second.  The copy does not depend
+    on the values, so the shards are zero-filled rather than drawn."""
+    import torch
+    import chain_synth as cs
+    import oracle
+    oracle.build()
+    u = cs.WORKLOADS["ulysses_128k"].dims
+    shards = torch.zeros((u["p"], u["n_loc"], u["H"], u["d"]), dtype=torch.bfloat16)
+    t0 = time.perf_counter()
+    out, _ = oracle.relayout(shards, u["p"], u["g"])
+    dt = time.perf_counter() - t0
+    return 2.0 * out.nbytes / dt / 1e9, dt
 
 
 def run_reference(args):
@@ -1158,8 +1184,13 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         v, s, desc, thr = oracle_sample()
+        rl_gbps, rl_s = oracle_relayout_gbps()
         cpu = {"value": v, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-               "sample": desc + f"; total {s:.1f}s"}
+               "sample": desc + f"; total {s:.1f}s",
+               # the whole step at the sample's rate (its relayouts aside)
+               "step_s_extrapolated": round(hp.flops / (v * 1e12), 1),
+               "relayout_GBps": round(rl_gbps, 2),
+               "relayout_sample": f"one full tensor, 536,870,912 B moved ({rl_s:.2f}s)"}
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
