@@ -478,6 +478,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tma_load_2d(dst + 16384, &tmW1, &full[s], c * HC2, t * KT);
           tma_load_2d(dst + 24576, &tmW1, &full[s], (c + CS) * HC2, t * KT);
         } else {      // W2 [hidden 64][out 256q..] as 4 boxes of 64 columns
+          // F16H: W2's f16 copy comes from the pre-pass, which this kernel
+          // may overlap (programmatic launch): wait for it before the first
+          // W2 tile; GEMM1's operands before it do not depend on it
+          if (F16H && c == 0) pdl_wait();
           mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
@@ -646,6 +650,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // O epilogue
     if (ok && mbar_wait(o_done, 0, p.wc, abort_flag, SITE_MLP_EPI)) {
       tc_fence_after();
+      if (F16H) pdl_wait();  // the pre-pass's scale (returns at once by now)
       const float os = F16H ? __ldg(p.w_inv) : 1.0f;
       __nv_bfloat16 *orow = p.O + (int64_t)(rb * BM + row) * p.P + q * BP;
 #pragma unroll 1
@@ -692,7 +697,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // 2^-31 of that maximum (f16 subnormals, absolute error at most 2^-39 of
 // it).  Two passes: WPB partial maxima, then each block reduces them,
 // converts its share and (block 0) stores 2^-k for the epilogue.
-constexpr int WPB = 1024;  // blocks of both passes (partial maxima of the first)
+constexpr int WPB = 256;   // blocks of both passes (partial maxima of the first): with the
+                           // main kernel all resident at once, so the launches overlap
 constexpr int WU = 4;      // 16-byte vectors in flight per thread and round
 
 __device__ __forceinline__ uint32_t block_max256(uint32_t v, uint32_t *red) {
@@ -709,6 +715,7 @@ __device__ __forceinline__ uint32_t block_max256(uint32_t v, uint32_t *red) {
 
 __global__ void __launch_bounds__(256)
     w_absmax_kernel(const uint4 *__restrict__ W, int64_t nvec, uint32_t *__restrict__ part) {
+  pdl_launch_dependents();  // the conversion may launch now; it waits for this grid
   __shared__ uint32_t red[8];
   const int64_t stride = (int64_t)gridDim.x * 256;
   uint32_t m = 0;
@@ -731,6 +738,10 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     w_to_f16_kernel(const uint4 *__restrict__ W, int64_t nvec, const uint32_t *__restrict__ part,
                     uint4 *__restrict__ out, float *__restrict__ w_inv) {
+  // the main kernel may begin launching now; it waits for this grid's
+  // completion before it reads the copy or the scale
+  pdl_launch_dependents();
+  pdl_wait();  // the partial maxima of w_absmax_kernel
   __shared__ uint32_t red[8];
   uint32_t m = 0;
 #pragma unroll
@@ -787,6 +798,8 @@ cudaError_t mlp_maps(const MlpArgs &a, const void *w2, CUtensorMapDataType w2_ty
   return cudaSuccess;
 }
 
+// F16H: launched to overlap the tail of its pre-pass (programmatic stream
+// serialization); the kernel waits for the pre-pass where it first needs W2.
 template <bool F16H>
 cudaError_t launch_cluster(const MlpArgs &a, const CUtensorMap &mx, const CUtensorMap &mw1,
                            const CUtensorMap &mw2, const float *w_inv, const WaitCfg &wc,
@@ -799,21 +812,20 @@ cudaError_t launch_cluster(const MlpArgs &a, const CUtensorMap &mx, const CUtens
   p.w_inv = w_inv;
   p.wc = wc;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(mlp_cluster_kernel<F16H>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, ClusterLayout::ALLOC)))
-    return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((a.M / BM) * CS));
   cfg.blockDim = dim3(NTHREADS);
   cfg.dynamicSmemBytes = ClusterLayout::ALLOC;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)CS;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = F16H ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, mlp_cluster_kernel<F16H>, mx, mw1, mw2, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -831,6 +843,9 @@ cudaError_t launch_mlp_chain(const MlpArgs &a, const WaitCfg &wc, cudaStream_t s
   cudaError_t e;
   if ((e = mlp_maps(a, a.W2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, &mx, &mw1, &mw2))) return e;
   if (cluster_shape(a)) {
+    if ((e = cudaFuncSetAttribute(mlp_cluster_kernel<false>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, ClusterLayout::ALLOC)))
+      return e;
     timing_mark(st, 0);
     e = launch_cluster<false>(a, mx, mw1, mw2, nullptr, wc, st);
     timing_mark(st, 1);
@@ -868,16 +883,36 @@ cudaError_t launch_mlp_chain_f16h(const MlpArgs &a, void *ws, const WaitCfg &wc,
   uint32_t *part = reinterpret_cast<uint32_t *>(base + wb);
   float *w_inv = reinterpret_cast<float *>(base + wb + 4 * WPB);
   const int64_t nvec = (int64_t)a.N * a.P / 8;  // P is a multiple of 256
+  // Host work first, so the main kernel's launch follows the pre-pass's
+  // closely enough to overlap its tail.
+  CUtensorMap mx, mw1, mw2;
+  cudaError_t e;
+  if ((e = mlp_maps(a, w16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, &mx, &mw1, &mw2))) return e;
+  if ((e = cudaFuncSetAttribute(mlp_cluster_kernel<true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, ClusterLayout::ALLOC)))
+    return e;
   timing_mark(st, 0);
   w_absmax_kernel<<<WPB, 256, 0, st>>>(static_cast<const uint4 *>(a.W2), nvec, part);
-  w_to_f16_kernel<<<WPB, 256, 0, st>>>(static_cast<const uint4 *>(a.W2), nvec, part, w16, w_inv);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  CUtensorMap mx, mw1, mw2;
-  if ((e = mlp_maps(a, w16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, &mx, &mw1, &mw2))) return e;
-  timing_mark(st, 1);
+  {
+    // the conversion launches while the maxima are still being taken
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(WPB);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, w_to_f16_kernel, static_cast<const uint4 *>(a.W2), nvec,
+                                static_cast<const uint32_t *>(part), w16, w_inv)))
+      return e;
+  }
+  if ((e = cudaGetLastError())) return e;
+  // no mark between the pre-pass and the main kernel: a recorded event there
+  // would keep them from overlapping
   e = launch_cluster<true>(a, mx, mw1, mw2, w_inv, wc, st);
-  timing_mark(st, 2);
+  timing_mark(st, 1);
   return e;
 }
 

@@ -153,6 +153,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *map, uint64_t
       : "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it in the stream is still running.  pdl_wait() returns
+// once that kernel has completed and its memory operations are visible (at
+// once when there is none in flight); pdl_launch_dependents() lets the next
+// kernel start launching before this one ends.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

@@ -471,8 +471,12 @@ void chain_set_wait_limit_ns(uint64_t ns);
  * k-th boundary of its main kernels: events[0] just before the first main
  * kernel, events[1] just after it, events[2] after the second (the
  * backward has two main kernels: dK/dV, then dQ; its small preprocess runs
- * before events[0]).  Boundaries beyond count are not recorded.  Pass
- * NULL, 0 to clear.  At most 4 events; events are owned by the caller.
+ * before events[0]).  The f16 forms count their pre-pass as the first
+ * main kernel, except chain_fwd_f16h: its main kernel may start while the
+ * pre-pass still runs, so it records events[0] before the pre-pass and
+ * events[1] after the main kernel only.  Boundaries beyond count are not
+ * recorded.  Pass NULL, 0 to clear.  At most 4 events; events are owned by
+ * the caller.
  */
 void chain_set_timing_events(void *const *events, int count);
 
