@@ -3,9 +3,10 @@
 Forward chains (bf16 in, fp32 accumulate): max|O - O_ref| <= 1e-2 max|O_ref|
 and mean relative error sum|O - O_ref| / sum|O_ref| <= 2e-3.  Gradients:
 ||dX - dX_ref||_F / ||dX_ref||_F <= 2e-2 for each of dQ, dK, dV.
-LSE (fp32, natural log): |LSE - LSE_ref| <= 1e-3 absolute (derivation in
-the design notes: fp32 score accumulation and ex2/lg2 approximation errors
-are ~1e-5; bf16 rounding of P does not enter the LSE).
+LSE (fp32, natural log): |LSE - LSE_ref| <= 1e-3 absolute.  The LSE is
+m + ln(l) from fp32 scores; fp32 accumulation of the scores and the
+ex2/lg2 approximations each contribute ~1e-5, and the rounding of P for the
+second product does not enter it, so 1e-3 leaves two orders of margin.
 The e4m3-input forward is held to the same bounds against the oracle fed the
 same codes (their exact values): its P is f16, its O one bf16 rounding.
 """
