@@ -109,6 +109,26 @@ def test_mlp_f16h_c_far_from_f16_range(cg, orc, w2_scale):
     assert_fwd_close(o, ref, f"f16h C x {w2_scale}")
 
 
+def test_mlp_f16h_back_to_back_calls_share_a_workspace(cg, orc):
+    # A call's main kernel overlaps its own pre-pass; the next call's pre-pass
+    # rewrites the same f16 copy and scale.  Two calls issued back to back
+    # (no synchronisation between them), with C differing by 2^10, must each
+    # match the oracle.
+    x, w1, w2 = cs.mlp_inputs(256, 128, 512, 512, seed=2450)
+    w2b = (w2.float() * 1024.0).to(torch.bfloat16)
+    xd, w1d = x.cuda(), w1.cuda()
+    w2d, w2bd = w2.cuda(), w2b.cuda()
+    ws = torch.empty(cg.chain_fwd_f16h_workspace_size(w2d), dtype=torch.uint8, device="cuda")
+    oa = torch.empty(256, 512, dtype=torch.bfloat16, device="cuda")
+    ob = torch.empty_like(oa)
+    for _ in range(3):
+        cg.chain_fwd_f16h(xd, w1d, w2d, cg.F_GELU_TANH, oa, ws)
+        cg.chain_fwd_f16h(xd, w1d, w2bd, cg.F_GELU_TANH, ob, ws)
+    assert cg.chain_check()[0] == 0
+    assert_fwd_close(oa, orc.chain_fwd(x, w1, w2, orc.F_GELU_TANH), "first call")
+    assert_fwd_close(ob, orc.chain_fwd(x, w1, w2b, orc.F_GELU_TANH), "second call")
+
+
 def test_mlp_f16h_matches_compensated_form(cg):
     # the two forms of the same chain agree to within their rounding
     x, w1, w2 = cs.mlp_inputs(512, 256, 512, 1024, seed=2500)
