@@ -127,7 +127,7 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=2)
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons, pw = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -138,14 +138,22 @@ class ClockSampler:
                 mx = float(f[2])
             except ValueError:
                 continue
+            try:
+                pw.append(float(f[3]))
+            except ValueError:
+                pass
             for nm, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["no samples"]}
         loaded = [s for s in sm if mx is None or s >= 0.3 * mx] or sm
+        # board power beside the clocks: the long attention kernels run at the
+        # power cap, which is what sets their clock
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_median": round(statistics.median(pw), 1) if pw else None,
+                "power_w_max": round(max(pw), 1) if pw else None}
 
 
 # ------------------------------------------------------------- the step
