@@ -153,7 +153,9 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx,
                 "reasons": sorted(reasons), "samples": len(sm),
                 "power_w_median": round(statistics.median(pw), 1) if pw else None,
-                "power_w_max": round(max(pw), 1) if pw else None}
+                "power_w_max": round(max(pw), 1) if pw else None,
+                "power_note": "nvidia-smi power.draw, an average over about its last second: "
+                              "it lags behind a timed region shorter than that"}
 
 
 # ------------------------------------------------------------- the step
