@@ -1121,6 +1121,10 @@ def main():
             for n_ in ("up", "comp", "down"):
                 out[f"{n_}_busy_ms"] = round(statistics.mean(
                     sum(el(a, b) for a, b in trace[k][n_]) for k in steps), 3)
+            # each traced step's upload time: the host side's throughput can
+            # swing within one run, which the mean alone hides
+            out["up_busy_ms_per_step"] = [round(sum(el(a, b) for a, b in trace[k]["up"]), 2)
+                                          for k in range(len(trace))]
 
             def wait(k, c):  # gap before component c of step k on the compute stream
                 prev_end = trace[k - 1]["comp"][-1][1] if c == 0 else trace[k]["comp"][c - 1][1]
@@ -1160,9 +1164,12 @@ def main():
         run(max(args.steps, 4), trace=trace)
         torch.cuda.synchronize()
         tl = timeline(trace)
+        # the link alone again: a change from before the run points at the host
+        # side (shared with other work on the machine), not at the pipeline
+        link_after = host_link_gbps(torch, dev)
         e2e = {"value": round(flops_all / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3),
-               "host_link_GBps": link,
+               "host_link_GBps": link, "host_link_GBps_after": link_after,
                "upload_floor_ms": round(h2d / (link["h2d"] * 1e9) * 1e3, 3),
                "timeline_per_step": tl,
                "overlap": "uploads and downloads on their own streams, double-buffered device sets; "
