@@ -879,22 +879,23 @@ def measure_varlen(hp, reps=5):
 
 
 def host_link_gbps(torch, dev, nbytes=1 << 30, reps=3):
-    """Pinned host <-> device copy bandwidth of this machine (best of reps,
-    one 1 GiB copy each way): the floor under the end-to-end figure."""
+    """Pinned host <-> device copy bandwidth of this machine (one 1 GiB copy
+    each way, reps times): the best is the floor under the end-to-end figure,
+    the worst shows how much the host side varies between copies."""
     h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     out = {}
     for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
-        best = None
+        times = []
         for _ in range(reps):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             dst.copy_(src, non_blocking=True)
             b.record()
             torch.cuda.synchronize()
-            ms = a.elapsed_time(b)
-            best = ms if best is None else min(best, ms)
-        out[name] = round(nbytes / (best * 1e-3) / 1e9, 1)
+            times.append(a.elapsed_time(b))
+        out[name] = round(nbytes / (min(times) * 1e-3) / 1e9, 1)
+        out[name + "_worst"] = round(nbytes / (max(times) * 1e-3) / 1e9, 1)
     del h, d
     return out
 
