@@ -1036,18 +1036,20 @@ def main():
     value = flops_all / (ms_step * 1e-3) / 1e12
 
     # ---- end to end through the C ABI with host buffers.  Every step copies
-    # its inputs from pinned host memory and its results back.  Two sets of
-    # device buffers let step k+1's uploads (own stream) run under step k's
-    # kernels, and step k's downloads (own stream) under step k+1's.  Each
+    # its inputs from pinned host memory and its results back.  NSET sets of
+    # device buffers let the uploads of the next steps (own stream) run under
+    # step k's kernels, and step k's downloads (own stream) under step k+1's;
+    # with three, a step whose uploads run slow (the host side's throughput
+    # can swing from step to step) is absorbed by the one before.  Each
     # component waits only for its own inputs, and its results leave as soon
     # as it has finished; events order each copy after the work whose
     # buffers it touches.
     e2e = None
+    NSET = 3
     if not args.no_e2e:
-        hps = [hp, HotPath(dev, only=args.only)]
+        hps = [hp] + [HotPath(dev, only=args.only) for _ in range(NSET - 1)]
         io0 = hp.host_io()
-        io1 = hps[1].host_io(make_host=False)
-        io = [io0, io1]
+        io = [io0] + [h.host_io(make_host=False) for h in hps[1:]]
         h2d = sum(t.numel() * t.element_size() for _, h_in, _, _ in io0 for t in h_in)
         d2h = sum(t.numel() * t.element_size() for _, _, _, h_out in io0 for t in h_out)
         s_up, s_down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
@@ -1058,21 +1060,21 @@ def main():
         def run(nsteps, t0=None, t1=None, trace=None):
             # trace: if a list, gets per step the host issue time and timing
             # events around each component's upload, compute and download
-            done = [ev(), ev()]   # step finished with its buffer set
-            down = [ev(), ev()]   # its results are on the host
+            done = [ev() for _ in range(NSET)]  # step finished with its buffer set
+            down = [ev() for _ in range(NSET)]  # its results are on the host
             tev = lambda: torch.cuda.Event(enable_timing=True)
             if t0 is not None:
                 t0.record(s_up)
             for k in range(nsteps):
                 h0 = time.perf_counter()
-                X = k % 2
+                X = k % NSET
                 up_c = [ev() for _ in range(ncomp)]
                 done_c = [ev() for _ in range(ncomp)]
                 tr = None if trace is None else {n_: [[tev(), tev()] for _ in range(ncomp)]
                                                  for n_ in ("up", "comp", "down")}
                 with torch.cuda.stream(s_up):
-                    if k >= 2:
-                        s_up.wait_event(done[X])  # step k-2 no longer reads these inputs
+                    if k >= NSET:
+                        s_up.wait_event(done[X])  # step k-NSET no longer reads these inputs
                     for c in range(ncomp):
                         if tr:
                             tr["up"][c][0].record(s_up)
@@ -1081,8 +1083,8 @@ def main():
                         up_c[c].record(s_up)
                         if tr:
                             tr["up"][c][1].record(s_up)
-                if k >= 2:
-                    comp.wait_event(down[X])  # step k-2's results are on the host
+                if k >= NSET:
+                    comp.wait_event(down[X])  # step k-NSET's results are on the host
                 with torch.cuda.stream(comp):
                     for c in range(ncomp):
                         comp.wait_event(up_c[c])
@@ -1149,7 +1151,7 @@ def main():
             out["step_detail_fields"] = "up start, up end, compute start, compute end, down start, down end"
             return out
 
-        run(2)
+        run(NSET)  # every buffer set used once before timing
         torch.cuda.synchronize()
         link = host_link_gbps(torch, dev)
         barrier(dist)
@@ -1173,7 +1175,7 @@ def main():
                "host_link_GBps": link, "host_link_GBps_after": link_after,
                "upload_floor_ms": round(h2d / (link["h2d"] * 1e9) * 1e3, 3),
                "timeline_per_step": tl,
-               "overlap": "uploads and downloads on their own streams, double-buffered device sets; "
+               "overlap": f"uploads and downloads on their own streams, {NSET} device buffer sets; "
                           "each component waits for its own inputs only and returns its results "
                           "as soon as it has finished"}
         rc, site = cg.chain_check()
