@@ -782,6 +782,46 @@ def _median_ms(torch, fn, reps, warm=2):
     return sorted(ts)[len(ts) // 2]
 
 
+def measure_sweep(torch, cg, dev, reps=5):
+    """Causal attention forward (chain_fwd_f16pv) and backward (chain_bwd) over
+    sequence lengths 2048 ... 131072 at a constant 1,048,576 (head, position)
+    pairs, for d = 128 and 64: how the rate holds up as the sequences shorten
+    and the heads multiply.  Run on its own (bench.py --sweep), not part of
+    the step."""
+    import chain_synth as cs
+    out = {}
+    for d in (128, 64):
+        for n in (2048, 8192, 32768, 131072):
+            BH = (1 << 20) // n
+            q, k, v, do = cs.attn_inputs(BH, n, d, seed=17000 + n + d, device=dev, with_do=True)
+            o = torch.empty_like(q)
+            lse = torch.empty(BH, n, dtype=torch.float32, device=dev)
+            wsf = torch.empty(max(cg.chain_fwd_f16pv_workspace_size(q, v), 16), dtype=torch.uint8,
+                              device=dev)
+            wsb = torch.empty(cg.chain_bwd_workspace_size(q, v), dtype=torch.uint8, device=dev)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            scale = d ** -0.5
+
+            def fwd():
+                cg.chain_fwd_f16pv(q, k, v, cg.MASK_CAUSAL, scale, o, lse, wsf)
+
+            def bwd():
+                cg.chain_bwd(do, q, k, v, o, lse, cg.F_SOFTMAX, cg.MASK_CAUSAL, scale, dq, dk, dv,
+                             wsb)
+
+            ms_f = _median_ms(torch, fwd, reps)
+            ms_b = _median_ms(torch, bwd, reps)
+            rc, site = cg.chain_check()
+            if rc != 0:
+                raise RuntimeError(f"device status {rc} site {site:#x} in the sweep")
+            ff, fb = attn_fwd_flops(BH, n, d, True), attn_bwd_flops(BH, n, d, True)
+            out[f"causal_{BH}x{n}x{d}"] = {
+                "fwd_ms": round(ms_f, 4), "fwd_TFLOPs": round(ff / (ms_f * 1e-3) / 1e12, 1),
+                "bwd_ms": round(ms_b, 4), "bwd_TFLOPs": round(fb / (ms_b * 1e-3) / 1e12, 1)}
+            del q, k, v, do, o, lse, wsf, wsb, dq, dk, dv
+    return out
+
+
 def measure_gqa(hp, reps=5):
     """Grouped-query attention, 32 query heads over 8 K/V heads at n = 32768,
     causal: forward (chain_fwd_f16pv) and backward (chain_bwd), each timed
@@ -910,6 +950,8 @@ def main():
     ap.add_argument("--only", default=None, help="substring: run only matching components")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="only the sequence-length / head-size sweep of the attention, one JSON line")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -924,6 +966,13 @@ def main():
     torch.cuda.set_device(dev)
     cg.lib()
     peaks, peak_src = load_peaks()
+    if args.sweep:
+        if rank == 0:
+            print(json.dumps({"sweep": measure_sweep(torch, cg, dev),
+                              "flops": "fwd 2 n^2 d BH, bwd 5 n^2 d BH (causal)",
+                              "timing": "median of 5 after 2 warm-ups",
+                              "calls": "chain_fwd_f16pv, chain_bwd"}))
+        return 0
     hp = HotPath(dev, only=args.only)
     stream = torch.cuda.current_stream()
     if not hp.comp:

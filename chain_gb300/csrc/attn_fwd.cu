@@ -92,6 +92,9 @@ struct FwdParams {
   const int *cu;
   int nbatch;
   int n_loc;  // positions per sequence shard (n when unsharded)
+  // causal, one sequence per head: the last tail_heads query heads' blocks run
+  // interleaved, heaviest first across them (1: strictly head by head)
+  int tail_heads;
   float scale_log2;
   float o_scale;  // f16 P V: factor applied with 1/l (8-bit inputs: 2^8 x the V scale)
   const float *v_inv;  // bf16 inputs with f16 P V: per K/V head 2^-k undoing V's scale
@@ -174,6 +177,15 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap &tmQ, const CUte
   if constexpr (!VARLEN) {
     bh = blk / p.nqb2;
     qb = p.causal ? (p.nqb2 - 1 - blk % p.nqb2) : (blk % p.nqb2);
+    // The last heads' heaviest blocks would otherwise start only when their
+    // own head comes up, and end the kernel after every other SM has gone
+    // idle; interleaving the final few heads starts them together.
+    const int first_tail = (p.BH - p.tail_heads) * p.nqb2;
+    if (p.causal && p.tail_heads > 1 && blk >= first_tail) {
+      const int r = blk - first_tail;
+      bh = p.BH - p.tail_heads + r % p.tail_heads;
+      qb = p.nqb2 - 1 - r / p.tail_heads;
+    }
   } else {
     // one sequence of a variable-length batch; bounds clamped to the packed
     // tensor so a bad cu can never address memory outside it.  Within a
@@ -761,6 +773,19 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+
+// Query heads whose blocks interleave at the end of a causal launch of one
+// sequence per head: as many as keep their K and V (a 16-bit copy each, at
+// most) under 64 MB of L2, in whole K/V-head groups.  Within the kernel, heads
+// otherwise run one after the other so each head's K and V stay in L2.
+int fwd_tail_heads(int BH, int BHkv, int64_t n, int d, bool causal, bool varlen) {
+  if (!causal || varlen || BHkv <= 0) return 1;
+  const int64_t kv = (int64_t(64) << 20) / (4 * n * d);
+  if (kv < 1) return 1;
+  const int64_t t = kv * (BH / BHkv);
+  return t < BH ? (int)t : BH;
+}
+
 template <int D>
 cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t st) {
   using L = FwdLayout<D, false>;
@@ -800,6 +825,7 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, const WaitCfg &wc, cudaStream_t s
   p.nqb2 = (nmax + 2 * BM - 1) / (2 * BM);
   p.nkb = (a.n + BN - 1) / BN;
   p.causal = a.causal;
+  p.tail_heads = fwd_tail_heads(a.BH, a.BHkv, a.n, D, a.causal, a.cu_seqlens != nullptr);
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.o_scale = 1.0f;
   p.v_inv = nullptr;
@@ -872,6 +898,7 @@ cudaError_t launch_attn_fwd_fp8(const AttnFwdArgs &a, void *v16, const WaitCfg &
   p.nqb2 = (a.n + 2 * BM - 1) / (2 * BM);
   p.nkb = (a.n + BN - 1) / BN;
   p.causal = a.causal;
+  p.tail_heads = fwd_tail_heads(a.BH, a.BHkv, a.n, 128, a.causal, false);
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.o_scale = 256.0f * a.v_scale;
   p.v_inv = nullptr;
@@ -959,6 +986,7 @@ static cudaError_t launch_pv16_d(const AttnFwdArgs &a, void *ws, const WaitCfg &
   p.nqb2 = nqb2;
   p.nkb = (a.n + BN - 1) / BN;
   p.causal = a.causal;
+  p.tail_heads = fwd_tail_heads(a.BH, a.BHkv, a.n, D, a.causal, a.cu_seqlens != nullptr);
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.o_scale = 1.0f;
   p.v_inv = v_inv;
